@@ -1,0 +1,373 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each test ties one oracle function to a library routine, a closed form, brute
+force on a tiny input, or an invariant of the quantized program, so that a
+dropped term, a wrong index or sign, or a transposed operand in the oracle
+fails here.  No expected value comes from the CUDA library.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+D = 128
+RNG = np.random.default_rng(20261202)
+
+
+def bf16(x):
+    """numbers -> bf16 bits through the library (torch) conversion"""
+    t = torch.tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16f(h):
+    return oracle.bf16_value(h)
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_library():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_value(codes)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert nan.sum() == 2  # S.1111.111 only
+    assert np.array_equal(ours[~nan], lib[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def _e4m3_probe_values():
+    finite = oracle.e4m3_value(np.arange(0, 0x7F, dtype=np.uint8))  # 0 .. 448
+    mids = (finite[:-1] + finite[1:]) / 2
+    pts = np.concatenate([finite, mids, [464.0, 465.0, 480.0, 1e4, 3e38, 1e-30, 2.0 ** -10]])
+    pts32 = pts.astype(np.float32)
+    up = np.nextafter(pts32, np.float32(np.inf))
+    dn = np.nextafter(pts32, np.float32(0))
+    rnd = RNG.uniform(0, 500, 20000).astype(np.float32)
+    tiny = (RNG.uniform(0, 2.0 ** -5, 20000)).astype(np.float32)
+    allv = np.concatenate([pts32, up, dn, rnd, tiny])
+    return np.concatenate([allv, -allv])
+
+
+def test_e4m3_encode_matches_library_rne_and_saturates():
+    x = _e4m3_probe_values()
+    ours = oracle.e4m3_value(oracle.f32_to_e4m3(x))
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    big = np.abs(x) > 464.0
+    assert np.array_equal(ours[~big], lib[~big])
+    assert np.all(np.abs(ours[big]) == 448.0)
+    assert np.array_equal(np.sign(ours[big]), np.sign(x[big]))
+
+
+def test_e4m3_encode_is_nearest_by_brute_force():
+    finite = oracle.e4m3_value(np.arange(0, 0x7F, dtype=np.uint8))
+    x = _e4m3_probe_values()
+    x = x[np.abs(x) <= 448.0]
+    got = np.abs(oracle.e4m3_value(oracle.f32_to_e4m3(x)))
+    a = np.abs(x.astype(np.float64))
+    dist = np.abs(a[:, None] - finite[None, :])
+    best = dist.min(axis=1)
+    assert np.all(np.abs(a - got) == best)
+    # ties go to the code with an even last mantissa bit
+    tie = np.sum(dist == best[:, None], axis=1) == 2
+    codes = oracle.f32_to_e4m3(x[tie]) & 0x7F
+    assert tie.sum() > 100 and np.all(codes % 2 == 0)
+
+
+def test_bf16_encode_matches_library():
+    bits = np.arange(0, 1 << 32, 4093, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x) & (np.abs(x) < 3e38)]
+    ours = oracle.f32_to_bf16(x)
+    lib = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, lib)
+
+
+def test_f16_decode_matches_library():
+    h = np.arange(1 << 16, dtype=np.uint16)
+    ours = oracle.f16_value(h)
+    lib = h.view(np.float16).astype(np.float64)
+    fin = np.isfinite(lib)
+    assert np.array_equal(ours[fin], lib[fin])
+    assert np.array_equal(np.isnan(ours), np.isnan(lib))
+
+
+# ---------------------------------------------------------------------------
+# K smoothing mean
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("nk", [1, 5, 255, 256, 257, 700])
+def test_k_mean_close_to_exact_mean(nk):
+    k = bf16(RNG.normal(0, 1, (nk, D)) + RNG.normal(0, 2, D)[None, :])
+    mu = oracle.k_mean(k).astype(np.float64)
+    kv = bf16f(k)
+    exact = np.array([math.fsum(kv[:, c]) / nk for c in range(D)])
+    bound = (nk + 2) * 2.0 ** -24 * np.abs(kv).max(axis=0) + 2.0 ** -24 * np.abs(exact)
+    assert np.all(np.abs(mu - exact) <= bound)
+    if nk == 1:
+        assert np.array_equal(mu, kv[0])
+
+
+def test_k_mean_constant_column_exact():
+    k = bf16(np.full((300, D), 1.5))
+    assert np.all(oracle.k_mean(k) == 1.5)
+
+
+# ---------------------------------------------------------------------------
+# Q/K INT8 per-block quantisation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,blk", [(1, 64), (63, 64), (129, 64), (300, 128)])
+def test_int8_quant_properties(n, blk):
+    q = bf16(RNG.normal(0, 1, (n, D)) * 3)
+    codes, scales = oracle.quant_q(q, blk)
+    x = bf16f(q)
+    assert scales.shape == ((n + blk - 1) // blk,)
+    assert np.abs(codes.astype(int)).max() <= 127
+    for b in range(scales.size):
+        blkx = x[b * blk:(b + 1) * blk]
+        blkc = codes[b * blk:(b + 1) * blk].astype(np.float64)
+        amax = np.abs(blkx).max()
+        # the block's largest magnitude lands on +-127
+        i = np.unravel_index(np.argmax(np.abs(blkx)), blkx.shape)
+        assert abs(blkc[i]) == 127 and np.sign(blkc[i]) == np.sign(blkx[i])
+        assert abs(scales[b] - amax / 127) <= 2.0 ** -23 * amax / 127
+        # reconstruction within half a step
+        err = np.abs(blkx - blkc * np.float64(scales[b]))
+        assert np.all(err <= (0.5 + 1e-4) * scales[b])
+
+
+def test_int8_quant_power_of_two_and_block_locality():
+    q = bf16(RNG.normal(0, 1, (200, D)))
+    c0, s0 = oracle.quant_q(q, 64)
+    for k in (-3, -1, 2, 3):
+        c1, s1 = oracle.quant_q(bf16(bf16f(q) * 2.0 ** k), 64)
+        assert np.array_equal(c0, c1)
+        assert np.array_equal(s1.astype(np.float64), s0.astype(np.float64) * 2.0 ** k)
+    # changing block 1 only changes block 1
+    x = bf16f(q).copy()
+    x[64:128] *= 5.0
+    c2, s2 = oracle.quant_q(bf16(x), 64)
+    keep = np.r_[0:64, 128:200]
+    assert np.array_equal(c2[keep], c0[keep])
+    assert s2[0] == s0[0] and np.array_equal(s2[2:], s0[2:]) and s2[1] != s0[1]
+
+
+def test_zero_block_gives_zero_scale_and_codes():
+    q = np.zeros((70, D), dtype=np.uint16)
+    c, s = oracle.quant_q(q, 64)
+    assert not c.any() and not s.any()
+
+
+def test_k_quant_uses_smoothed_values():
+    k = bf16(RNG.normal(0, 1, (130, D)) + 40.0)
+    mu = oracle.k_mean(k)
+    c, s = oracle.quant_k(k, 64, mu)
+    # after removing the ~40 mean the step is set by the spread (~4), not by ~44
+    assert s.max() < 6.0 / 127
+    recon = c.astype(np.float64) * np.repeat(s, 64)[:130, None] + mu[None, :]
+    assert np.abs(recon - bf16f(k)).max() <= 0.51 * s.max() + 1e-5
+
+
+# ---------------------------------------------------------------------------
+# V FP8 per-channel quantisation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("nk", [1, 100, 128, 257])
+def test_fp8_v_quant_properties(nk):
+    v = bf16(RNG.normal(0, 1, (nk, D)) * np.exp(RNG.normal(0, 1, D))[None, :])
+    codes, sv = oracle.quant_v(v)
+    x = bf16f(v)
+    assert codes.shape == (D, oracle.nk_pad(nk))
+    assert not codes[:, nk:].any()
+    val = oracle.e4m3_value(codes[:, :nk]).T  # [nk, D]
+    amax = np.abs(x).max(axis=0)
+    assert np.all(np.abs(sv - amax / 448) <= 2.0 ** -23 * amax / 448)
+    i = np.argmax(np.abs(x), axis=0)
+    assert np.all(np.abs(val[i, np.arange(D)]) == 448.0)
+    scaled = x / sv[None, :].astype(np.float64)
+    normal = np.abs(scaled) >= 2.0 ** -6
+    rel = np.abs(val - scaled) / np.maximum(np.abs(scaled), 1e-30)
+    assert np.all(rel[normal] <= 2.0 ** -4 * (1 + 1e-5))
+    assert np.all(np.abs(val - scaled)[~normal] <= 2.0 ** -10 * (1 + 1e-5))
+
+
+def test_fp8_v_quant_power_of_two():
+    v = bf16(RNG.normal(0, 1, (150, D)))
+    c0, s0 = oracle.quant_v(v)
+    c1, s1 = oracle.quant_v(bf16(bf16f(v) * 8.0))
+    assert np.array_equal(c0, c1) and np.array_equal(s1, s0 * 8)
+
+
+# ---------------------------------------------------------------------------
+# the attention program
+# ---------------------------------------------------------------------------
+
+def softmax_attn_f64(q, k, v, sm):
+    s = (q @ k.T) * sm
+    s -= s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    return (p / p.sum(axis=1, keepdims=True)) @ v
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 1), (5, 127), (3, 128), (7, 129), (4, 300)])
+@pytest.mark.parametrize("tile", [1, 7, 128, 1000])
+def test_tile_loop_equals_bruteforce_softmax_when_unquantised(nq, nk, tile):
+    q = RNG.normal(0, 1, (nq, D))
+    k = RNG.normal(0, 1, (nk, D)) * 1.5
+    v = RNG.normal(0, 1, (nk, D))
+    sm = 1 / math.sqrt(D)
+    ours = oracle.attn_rows_f64(q, k, v, sm, tile)
+    ref = softmax_attn_f64(q, k, v, sm)
+    assert np.abs(ours - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def quantized_head(q, k, v, blk=64):
+    return oracle.sage_head(q, k, v, blk, blk, nthreads=1)
+
+
+def f64_attention(q, k, v):
+    return softmax_attn_f64(bf16f(q), bf16f(k), bf16f(v), 1 / math.sqrt(D))
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def test_single_key_returns_dequantised_v_row():
+    q = bf16(RNG.normal(0, 1, (9, D)))
+    k = bf16(RNG.normal(0, 1, (1, D)))
+    v = bf16(RNG.normal(0, 1, (1, D)))
+    r = quantized_head(q, k, v)
+    assert not r["kc"].any() and r["sk"][0] == 0.0
+    vdeq = oracle.e4m3_value(r["vct"][:, 0]) * r["sv"].astype(np.float64)
+    for row in r["out"]:
+        assert np.all(np.abs(row - vdeq) <= 2.0 ** -22 * np.abs(vdeq))
+
+
+@pytest.mark.parametrize("nk", [1, 64, 127, 129, 257])
+def test_zero_query_averages_dequantised_v(nk):
+    q = np.zeros((3, D), dtype=np.uint16)
+    k = bf16(RNG.normal(0, 1, (nk, D)))
+    v = bf16(RNG.normal(0, 1, (nk, D)))
+    r = quantized_head(q, k, v)
+    vdeq = oracle.e4m3_value(r["vct"][:, :nk]).T * r["sv"][None, :].astype(np.float64)
+    mean = vdeq.mean(axis=0)
+    for row in r["out"]:
+        assert np.all(np.abs(row - mean) <= 1e-6 * np.abs(vdeq).max())
+
+
+def test_bit_exact_invariants_of_the_quantized_program():
+    q = bf16(RNG.normal(0, 1, (70, D)))
+    k = bf16(RNG.normal(0, 1, (200, D)) + RNG.normal(0, 2, D)[None, :])
+    v = bf16(RNG.normal(0, 1, (200, D)))
+    base = quantized_head(q, k, v)["out"].astype(np.float64)
+    for e in (-3, -1, 2, 3):
+        out_v = quantized_head(q, k, bf16(bf16f(v) * 2.0 ** e))["out"].astype(np.float64)
+        assert np.array_equal(out_v, base * 2.0 ** e)
+        out_qk = quantized_head(bf16(bf16f(q) * 2.0 ** e), bf16(bf16f(k) * 2.0 ** -e), v)["out"]
+        assert np.array_equal(out_qk.astype(np.float64), base)
+
+
+def test_close_to_fp64_attention_on_the_tiny_workload():
+    w = synth.dense_workload("tiny_b1h2n256")
+    x = synth.dense_inputs(w)
+    for h in range(w.H):
+        out = quantized_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.block)["out"]
+        assert rel_l2(out, f64_attention(x["q"][0, h], x["k"][0, h], x["v"][0, h])) <= 5e-2
+
+
+def test_per_block_and_per_channel_scales_are_applied_where_they_belong():
+    nq, nk = 192, 256
+    q = RNG.normal(0, 1, (nq, D)) * np.repeat(2.0 ** np.array([0, 2, -1]), 64)[:, None]
+    k = RNG.normal(0, 1, (nk, D)) * np.repeat(2.0 ** np.array([1, -2, 0, 3]), 64)[:, None] / 2
+    v = RNG.normal(0, 1, (nk, D)) * (2.0 ** (np.arange(D) % 5))[None, :]
+    q, k, v = bf16(q), bf16(k), bf16(v)
+    out = quantized_head(q, k, v)["out"]
+    assert rel_l2(out, f64_attention(q, k, v)) <= 5e-2
+
+
+def test_k_smoothing_removes_a_large_channel_offset():
+    q = bf16(RNG.normal(0, 1, (64, D)))
+    # quarter-integers in [-3.75, 3.75]: K and K + 48 are both exact in bf16
+    kr = np.clip(np.round(RNG.normal(0, 1, (256, D)) * 4) / 4, -3.75, 3.75)
+    v = bf16(RNG.normal(0, 1, (256, D)))
+    k0 = bf16(kr)
+    k1 = bf16(kr + 48.0 * RNG.choice([-1.0, 1.0], D)[None, :])
+    assert np.array_equal(bf16f(k1) - bf16f(k0), np.round(bf16f(k1) - bf16f(k0)))
+    o0 = quantized_head(q, k0, v)["out"]
+    o1 = quantized_head(q, k1, v)["out"]
+    # softmax ignores a per-channel shift of K; with smoothing so does the program
+    # (an unsmoothed step of ~52/127 would put it far off the fp64 result)
+    assert rel_l2(o1, f64_attention(q, k1, v)) <= 5e-2
+    assert rel_l2(o1, o0) <= 1e-2
+
+
+# ---------------------------------------------------------------------------
+# int8 KV-cache prompt attention (fp64 exact program)
+# ---------------------------------------------------------------------------
+
+def _dequant(codes, scales):
+    return codes.astype(np.float64) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def test_int8kv_zero_query_is_the_causal_mean_per_group():
+    Nq, Nk, Hq, Hkv = 6, 20, 4, 2
+    p0 = Nk - Nq
+    q = np.zeros((Nq, Hq, D), dtype=np.uint16)
+    kc = RNG.integers(-127, 128, (Hkv, Nk, D)).astype(np.int8)
+    vc = RNG.integers(-127, 128, (Hkv, Nk, D)).astype(np.int8)
+    ks = RNG.uniform(0.01, 0.05, (Hkv, Nk)).astype(np.float16)
+    vs = RNG.uniform(0.01, 0.05, (Hkv, Nk)).astype(np.float16)
+    rows, heads = np.meshgrid(np.arange(Nq), np.arange(Hq), indexing="ij")
+    out, _ = oracle.int8kv_rows(q, kc, ks, vc, vs, p0, rows.ravel(), heads.ravel(), nthreads=1)
+    vdeq = _dequant(vc, vs)
+    for n, (i, h) in enumerate(zip(rows.ravel(), heads.ravel())):
+        g = h // (Hq // Hkv)
+        expect = vdeq[g, :p0 + i + 1].mean(axis=0)
+        assert np.abs(out[n] - expect).max() <= 1e-12
+
+
+def test_int8kv_dominant_key_is_selected():
+    Nq, Nk, Hq, Hkv = 4, 50, 2, 1
+    p0 = Nk - Nq
+    kc = np.zeros((Hkv, Nk, D), dtype=np.int8)
+    target = 17
+    kc[0, target, 3] = 127
+    ks = np.full((Hkv, Nk), 0.02, dtype=np.float16)
+    vc = RNG.integers(-127, 128, (Hkv, Nk, D)).astype(np.int8)
+    vs = RNG.uniform(0.01, 0.05, (Hkv, Nk)).astype(np.float16)
+    qv = np.zeros((Nq, Hq, D), dtype=np.float32)
+    qv[:, :, 3] = 200.0
+    out, _ = oracle.int8kv_rows(bf16(qv), kc, ks, vc, vs, p0, [0, 3], [0, 1], nthreads=1)
+    expect = _dequant(vc, vs)[0, target]
+    assert np.abs(out - expect[None, :]).max() <= 1e-9 * np.abs(expect).max()
+
+
+def test_int8kv_scale_exchange_and_group_sharing():
+    w = synth.int8kv_workload("tiny_kv_q96_k300")
+    x = synth.int8kv_inputs(w)
+    rows = np.array([0, 5, 95, 95, 40])
+    heads = np.array([0, 3, 7, 4, 1])
+    base, _ = oracle.int8kv_rows(x["q"], x["k"], x["k_scale"], x["v"], x["v_scale"], w.q_pos0,
+                                 rows, heads, nthreads=1)
+    # q * 4 with key scales / 4: identical logits
+    q4 = bf16(bf16f(x["q"]) * 4.0)
+    ks4 = (x["k_scale"].astype(np.float32) / 4).astype(np.float16)
+    alt, _ = oracle.int8kv_rows(q4, x["k"], ks4, x["v"], x["v_scale"], w.q_pos0, rows, heads,
+                                nthreads=1)
+    assert np.abs(alt - base).max() <= 1e-12
+    # two query heads of one group with the same q row give the same output
+    q2 = x["q"].copy()
+    q2[:, 1] = q2[:, 0]
+    o2, _ = oracle.int8kv_rows(q2, x["k"], x["k_scale"], x["v"], x["v_scale"], w.q_pos0,
+                               [10, 10], [0, 1], nthreads=1)
+    assert np.array_equal(o2[0], o2[1])
