@@ -141,7 +141,9 @@ uint8_t orc_f32_to_e4m3(float xf)
             code = (uint8_t)((E << 3) | M);
         }
     }
-    if (signbit(x) && r > 0.0) code |= 0x80u;
+    /* the format has a signed zero: a negative input that rounds to zero
+       keeps its sign (code 0x80), as round-to-nearest does in IEEE formats */
+    if (signbit(x)) code |= 0x80u;
     return code;
 }
 

@@ -59,10 +59,16 @@ def _e4m3_probe_values():
 
 def test_e4m3_encode_matches_library_rne_and_saturates():
     x = _e4m3_probe_values()
-    ours = oracle.e4m3_value(oracle.f32_to_e4m3(x))
+    codes = oracle.f32_to_e4m3(x)
+    ours = oracle.e4m3_value(codes)
+    lib_codes = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     lib = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
     big = np.abs(x) > 464.0
+    # code bits, so the sign of a zero result counts too
+    assert np.array_equal(codes[~big], lib_codes[~big])
     assert np.array_equal(ours[~big], lib[~big])
+    tiny_neg = (x < 0) & (x > -(2.0 ** -10))
+    assert tiny_neg.any() and np.all(codes[tiny_neg] == 0x80)
     assert np.all(np.abs(ours[big]) == 448.0)
     assert np.array_equal(np.sign(ours[big]), np.sign(x[big]))
 
