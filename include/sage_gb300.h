@@ -1,0 +1,177 @@
+/*
+ * sage_gb300.h - C ABI of the GB300 (sm_103a) quantized attention library.
+ *
+ * The library computes the data-parallel hot path of SageAttention-2-style
+ * quantized attention and of int8 KV-cache prompt attention.  Everything runs
+ * in the library's own CUDA kernels on the caller's stream.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory and never synchronises the stream.  Scratch
+ *    memory, where an entry point needs some, is passed in by the caller; its
+ *    size comes from the matching *_workspace() query.
+ *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ *    default stream).  Work is enqueued asynchronously.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    are returned as SAGE_ERR_INVALID_ARG or SAGE_ERR_UNSUPPORTED; nothing is
+ *    written in that case.  A failed launch returns SAGE_ERR_CUDA.
+ *  - `status_dev`, where present, may be NULL.  Otherwise it is a device int32
+ *    that kernels set (atomically, never clear) to a non-zero sage_status when
+ *    they detect a condition on the device, e.g. SAGE_ERR_TIMEOUT when a
+ *    bounded wait inside a kernel ran out.  The caller zeroes it and reads it
+ *    after synchronising.
+ *  - Head dimension d must be 128.  Element strides describe [B, H, N, d]
+ *    tensors whose channel stride is 1; every stride and base pointer must be
+ *    16-byte aligned (strides are multiples of 8 elements for bf16).
+ *  - Inputs must be finite.  The functions hold no global state and may be
+ *    called from several host threads.
+ *
+ * Citations name the page and its section that defines each operation.
+ */
+#ifndef SAGE_GB300_H
+#define SAGE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int sage_status;
+#define SAGE_OK 0
+#define SAGE_ERR_INVALID_ARG 1  /* null/misaligned pointer, bad size or stride   */
+#define SAGE_ERR_UNSUPPORTED 2  /* d != 128, block size not 64/128, and the like  */
+#define SAGE_ERR_CUDA 3         /* a CUDA call or kernel launch failed            */
+#define SAGE_ERR_WORKSPACE 4    /* workspace smaller than the *_workspace() size  */
+#define SAGE_ERR_TIMEOUT 5      /* device side: a bounded wait ran out            */
+
+/* Element strides of a [B, H, N, 128] tensor (channel stride is 1). */
+typedef struct {
+    int64_t b, h, n;
+} sage_strides;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *sage_status_string(sage_status s);
+
+/* Version of this ABI (bumped on any incompatible change). */
+int sage_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * sage_quantize_qk - K smoothing, then INT8 per-block quantisation of Q and
+ * of the smoothed K.
+ *
+ * Defines: "H3 Performance Roadmap", section "Measured GB10 Baseline", table
+ * "SageAttention 2.2.0 internals" (rows "Q/K INT8 quantization" and "K
+ * smoothing"), and section "Phase 4: Dense Sage-Compatible Attention", items
+ * 2-3 (keep the per-block INT8 Q/K policy and K smoothing).
+ *
+ * Computes, per (b, h):
+ *   k_mean[c]  = mean of K[t, c] over t < Nk: tokens summed in ascending
+ *                order in fp32 inside chunks of 256, chunk sums added in
+ *                ascending order in fp32, the total divided by Nk;
+ *   Ks         = fl(K - k_mean)  (fp32);
+ *   per block of `q_block` (`k_block`) tokens, the last one partial:
+ *   scale      = fl(amax / 127), amax = max |x| over the block;
+ *   code       = clamp(rint_even(fl(x * fl(127 / amax))), -127, 127),
+ *                0 everywhere when amax = 0.
+ * Inputs : q_bf16 [B,H,Nq,128] with strides qs; k_bf16 [B,H,Nk,128] with ks.
+ * Outputs (contiguous): q_codes int8 [B,H,Nq,128]; q_scales fp32
+ *   [B,H,ceil(Nq/q_block)]; k_codes int8 [B,H,Nk,128]; k_scales fp32
+ *   [B,H,ceil(Nk/k_block)]; k_mean fp32 [B,H,128].
+ * q_block, k_block in {64, 128}.  Nq, Nk >= 1.  Workspace: at least
+ * sage_quantize_qk_workspace(B, H, Nk) bytes, 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t sage_quantize_qk_workspace(int B, int H, int Nk);
+sage_status sage_quantize_qk(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                             int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
+                             int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                             float *k_mean, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sage_quantize_v - FP8 E4M3 per-channel quantisation of V, written
+ * transposed for the P.V product.
+ *
+ * Defines: "H3 Performance Roadmap", section "Measured GB10 Baseline", table
+ * "SageAttention 2.2.0 internals" (row "V FP8 quantization") and the
+ * uninstrumented phase list of the Sage2 decomposition ("V transpose/
+ * quantization").
+ *
+ * Per (b, h, channel c): amax_c = max_t |V[t, c]|; v_scales[c] = fl(amax_c/448);
+ * code = e4m3_rn_satfinite(fl(V * fl(448/amax_c))) (OCP E4M3, largest finite
+ * 448), 0 when amax_c = 0.
+ * Input : v_bf16 [B,H,Nk,128] with strides vs.
+ * Outputs (contiguous): v_codes uint8 [B,H,128,Nk_pad] with
+ *   Nk_pad = ceil(Nk/128)*128 and codes 0 for tokens >= Nk;
+ *   v_scales fp32 [B,H,128].
+ * Workspace: at least sage_quantize_v_workspace(B, H, Nk) bytes.
+ * ---------------------------------------------------------------------- */
+size_t sage_quantize_v_workspace(int B, int H, int Nk);
+sage_status sage_quantize_v(const void *v_bf16, sage_strides vs, int B, int H, int Nk, int d,
+                            uint8_t *v_codes, float *v_scales, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sage_attn_fwd - non-causal quantized attention forward over the outputs of
+ * sage_quantize_qk / sage_quantize_v.
+ *
+ * Defines: "Sage2 SM89 Temporal Pair Experiment", section "Candidate" (per
+ * KV tile the order QK -> online-softmax update of m, d, O -> accumulate the
+ * denominator -> scores to FP8 -> PV; V scale fused into the epilogue, kernel
+ * name "..._fuse_v_scale_attn_inst_buf"), and "H3 Performance Roadmap",
+ * section "Phase 4: Dense Sage-Compatible Attention".
+ *
+ * For each query row i and 128-key tile (ascending):
+ *   S = q_codes . k_codes (exact int32), s = S * fl(fl(sq*sk) * C) with
+ *   C = fl(sm_scale * log2 e); m' = max(m, max s); alpha = 2^(m - m');
+ *   p = 2^(s - m'); l = alpha*l + sum p (fp32 p); P = e4m3(448 p);
+ *   O = alpha*O + P.V (fp32 accumulate); out = bf16(O / l * v_scale / 448).
+ * Inputs: codes/scales as written by the two quantisers (q_block, k_block
+ *   must match), Nk_pad as there.  sm_scale <= 0 selects 1/sqrt(128).
+ * Output: out_bf16 [B,H,Nq,128] with element strides os.
+ * Workspace: at least sage_attn_fwd_workspace(B, H, Nq, Nk) bytes (fp16
+ *   images of the int8 codes for the tensor cores).
+ * ---------------------------------------------------------------------- */
+size_t sage_attn_fwd_workspace(int B, int H, int Nq, int Nk);
+sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                          const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                          int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
+                          float sm_scale, void *out_bf16, sage_strides os, void *workspace,
+                          size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/* ------------------------------------------------------------------------
+ * int8kv_prompt_attn - causal prompt attention of bf16 queries over an int8
+ * KV cache with per-token fp16 scales, grouped-query heads.
+ *
+ * Defines: "Strata PR #2092" (sm_75 v2 int8 prompt attention), its
+ * description (chunked prompt attention over the int8 KV cache, per-chunk
+ * K/V staging with their scales) and its table "qsa_prompt_attn_parity (int8
+ * KV), ms per chunk and error against FP64"; "Strata PR #2146" (the same
+ * kernel in one stage).
+ *
+ * Query i (absolute position q_pos0 + i) of query head h reads kv head
+ * g = h / (Hq / Hkv) and keys j <= q_pos0 + i:
+ *   s_ij = sm_scale * ks_j * sum_c q_ic kc_jc;  p = softmax_j(s) in fp32;
+ *   out_ic = sum_j p_ij * vs_j * vc_jc.
+ * Layouts: q_bf16 [Nq, Hq, 128] with element strides q_tok_stride (between
+ *   tokens) and q_head_stride (between heads); k_cache, v_cache int8
+ *   [Hkv, Nk, 128] with kv_head_stride elements between heads and 128 between
+ *   tokens; k_scale_f16, v_scale_f16 fp16 [Hkv, Nk] with scale_head_stride;
+ *   out_bf16 [Nq, Hq, 128] with o_tok_stride, o_head_stride.
+ * Requires Hq % Hkv == 0, 1 <= Nq, q_pos0 >= 0, q_pos0 + Nq <= Nk.
+ * sm_scale <= 0 selects 1/sqrt(128).  Workspace: at least
+ * int8kv_prompt_attn_workspace(Nq, Hq, Hkv, Nk) bytes.
+ * ---------------------------------------------------------------------- */
+size_t int8kv_prompt_attn_workspace(int Nq, int Hq, int Hkv, int Nk);
+sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
+                               const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
+                               const void *v_scale_f16, int64_t kv_head_stride,
+                               int64_t scale_head_stride, int Nq, int q_pos0, int Nk, int Hq,
+                               int Hkv, int d, float sm_scale, void *out_bf16, int64_t o_tok_stride,
+                               int64_t o_head_stride, void *workspace, size_t workspace_bytes,
+                               int32_t *status_dev, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SAGE_GB300_H */

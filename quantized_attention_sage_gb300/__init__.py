@@ -1,0 +1,237 @@
+"""GB300 (sm_103a) quantized attention: Python binding of ``libsage_gb300.so``.
+
+This module only marshals arguments: it turns torch tensors into device
+pointers, element strides and the current CUDA stream, allocates outputs and
+workspaces with torch, and calls the C ABI declared in
+``include/sage_gb300.h``.  Every step of the computation runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback.  If the library has not
+been built (``build()``), every call raises.
+
+Entry points (same names as the C ABI):
+  sage_quantize_qk, sage_quantize_v, sage_attn_fwd, int8kv_prompt_attn
+plus ``sage_attention`` (the three dense steps in a row).
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import math
+import os
+
+from .build import LIB, build as _build_lib
+
+__all__ = [
+    "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
+    "int8kv_prompt_attn", "sage_attention", "Strides", "STATUS",
+]
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+          4: "workspace too small", 5: "bounded device wait timed out"}
+D = 128
+
+
+class SageError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, 'unknown')} (status {code})")
+        self.code = code
+
+
+class Strides(C.Structure):
+    _fields_ = [("b", C.c_int64), ("h", C.c_int64), ("n", C.c_int64)]
+
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree) and load it."""
+    global _lib
+    path = _build_lib(force=force)
+    _lib = None
+    lib()
+    return path
+
+
+def lib():
+    """The loaded C library with argument types set; raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB):
+        raise RuntimeError(f"{LIB} is missing: the CUDA library must be built (call build())")
+    L = C.CDLL(LIB)
+    vp, i32, i64, sz, f32 = C.c_void_p, C.c_int, C.c_int64, C.c_size_t, C.c_float
+    L.sage_status_string.restype = C.c_char_p
+    L.sage_status_string.argtypes = [i32]
+    L.sage_abi_version.restype = i32
+    L.sage_quantize_qk_workspace.restype = sz
+    L.sage_quantize_qk_workspace.argtypes = [i32, i32, i32]
+    L.sage_quantize_qk.restype = i32
+    L.sage_quantize_qk.argtypes = [vp, Strides, vp, Strides, i32, i32, i32, i32, i32, i32, i32,
+                                   vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sage_quantize_v_workspace.restype = sz
+    L.sage_quantize_v_workspace.argtypes = [i32, i32, i32]
+    L.sage_quantize_v.restype = i32
+    L.sage_quantize_v.argtypes = [vp, Strides, i32, i32, i32, i32, vp, vp, vp, sz, vp]
+    L.sage_attn_fwd_workspace.restype = sz
+    L.sage_attn_fwd_workspace.argtypes = [i32, i32, i32, i32]
+    L.sage_attn_fwd.restype = i32
+    L.sage_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                vp, Strides, vp, sz, vp, vp]
+    L.int8kv_prompt_attn_workspace.restype = sz
+    L.int8kv_prompt_attn_workspace.argtypes = [i32, i32, i32, i32]
+    L.int8kv_prompt_attn.restype = i32
+    L.int8kv_prompt_attn.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32,
+                                     i32, f32, vp, i64, i64, vp, sz, vp, vp]
+    _lib = L
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _strides4(t) -> Strides:
+    if t.dim() != 4 or t.shape[3] != D or t.stride(3) != 1:
+        raise ValueError("expected a [B, H, N, 128] tensor with unit channel stride")
+    return Strides(t.stride(0), t.stride(1), t.stride(2))
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SageError(code, where)
+
+
+def _workspace(nbytes: int, device, ws=None):
+    torch = _torch()
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        return ws
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------
+# dense path
+# ---------------------------------------------------------------------------
+
+def sage_quantize_qk(q, k, q_block: int = 64, k_block: int = 64, out=None, workspace=None, stream=None):
+    """INT8 per-block codes of Q and of the mean-smoothed K.
+
+    q: [B,H,Nq,128] bf16, k: [B,H,Nk,128] bf16 (any 16-byte aligned strides).
+    Returns dict(q_codes, q_scales, k_codes, k_scales, k_mean)."""
+    torch = _torch()
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
+    dev = q.device
+    if out is None:
+        out = dict(
+            q_codes=torch.empty((B, H, Nq, D), dtype=torch.int8, device=dev),
+            q_scales=torch.empty((B, H, -(-Nq // q_block)), dtype=torch.float32, device=dev),
+            k_codes=torch.empty((B, H, Nk, D), dtype=torch.int8, device=dev),
+            k_scales=torch.empty((B, H, -(-Nk // k_block)), dtype=torch.float32, device=dev),
+            k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev))
+    L = lib()
+    nbytes = L.sage_quantize_qk_workspace(B, H, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_quantize_qk(_ptr(q), _strides4(q), _ptr(k), _strides4(k), B, H, Nq, Nk, D, q_block,
+                              k_block, _ptr(out["q_codes"]), _ptr(out["q_scales"]), _ptr(out["k_codes"]),
+                              _ptr(out["k_scales"]), _ptr(out["k_mean"]), _ptr(ws), nbytes,
+                              _stream(stream)), "sage_quantize_qk")
+    return out
+
+
+def nk_pad(nk: int) -> int:
+    return (nk + 127) // 128 * 128
+
+
+def sage_quantize_v(v, out=None, workspace=None, stream=None):
+    """FP8 E4M3 per-channel codes of V, transposed to [B,H,128,Nk_pad], and scales [B,H,128]."""
+    torch = _torch()
+    B, H, Nk, _ = v.shape
+    dev = v.device
+    if out is None:
+        out = dict(v_codes=torch.empty((B, H, D, nk_pad(Nk)), dtype=torch.uint8, device=dev),
+                   v_scales=torch.empty((B, H, D), dtype=torch.float32, device=dev))
+    L = lib()
+    nbytes = L.sage_quantize_v_workspace(B, H, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_quantize_v(_ptr(v), _strides4(v), B, H, Nk, D, _ptr(out["v_codes"]), _ptr(out["v_scales"]),
+                             _ptr(ws), nbytes, _stream(stream)), "sage_quantize_v")
+    return out
+
+
+def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
+                  out=None, workspace=None, status=None, stream=None):
+    """Quantized attention forward over the two quantisers' outputs; bf16 [B,H,Nq,128]."""
+    torch = _torch()
+    qc, kc = qk["q_codes"], qk["k_codes"]
+    B, H, Nq, _ = qc.shape
+    Nk = kc.shape[2]
+    dev = qc.device
+    if out is None:
+        out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=dev)
+    L = lib()
+    nbytes = L.sage_attn_fwd_workspace(B, H, Nq, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_attn_fwd(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
+                           _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
+                           float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
+                           _stream(stream)), "sage_attn_fwd")
+    return out
+
+
+def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,
+                   stream=None):
+    """The dense path in one call: quantize Q/K, quantize V, attention."""
+    qk = sage_quantize_qk(q, k, q_block, k_block, stream=stream)
+    vq = sage_quantize_v(v, stream=stream)
+    return sage_attn_fwd(qk, vq, q_block, k_block, sm_scale, out=out, stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# int8 KV-cache prompt attention
+# ---------------------------------------------------------------------------
+
+def int8kv_prompt_attn(q, k_cache, k_scale, v_cache, v_scale, q_pos0: int, sm_scale: float = 0.0,
+                       out=None, workspace=None, status=None, stream=None):
+    """Causal prompt attention of q [Nq,Hq,128] bf16 over an int8 cache.
+
+    k_cache, v_cache: int8 [Hkv, Nk, 128] (token rows contiguous);
+    k_scale, v_scale: fp16 [Hkv, Nk].  Returns bf16 [Nq, Hq, 128]."""
+    torch = _torch()
+    Nq, Hq, _ = q.shape
+    Hkv, Nk, _ = k_cache.shape
+    if k_cache.stride() != v_cache.stride() or k_cache.stride(1) != D or k_cache.stride(2) != 1:
+        raise ValueError("k_cache and v_cache must share a [Hkv, Nk, 128] layout with contiguous token rows")
+    if k_scale.stride() != v_scale.stride() or k_scale.stride(1) != 1:
+        raise ValueError("k_scale and v_scale must share a [Hkv, Nk] layout")
+    if q.stride(2) != 1:
+        raise ValueError("q channel stride must be 1")
+    dev = q.device
+    if out is None:
+        out = torch.empty((Nq, Hq, D), dtype=torch.bfloat16, device=dev)
+    L = lib()
+    nbytes = L.int8kv_prompt_attn_workspace(Nq, Hq, Hkv, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.int8kv_prompt_attn(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(k_scale),
+                                _ptr(v_cache), _ptr(v_scale), k_cache.stride(0), k_scale.stride(0), Nq,
+                                int(q_pos0), Nk, Hq, Hkv, D, float(sm_scale), _ptr(out), out.stride(0),
+                                out.stride(1), _ptr(ws), nbytes, _ptr(status), _stream(stream)),
+           "int8kv_prompt_attn")
+    return out
+
+
+def default_sm_scale() -> float:
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,214 @@
+// C ABI of the library: argument validation, workspace sizing, tensor-map
+// encoding and the launches.  Declarations and their contracts are in
+// include/sage_gb300.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace sg {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled tensor map, 128-byte swizzle, zero fill outside the tensor.
+bool encode_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                    uint32_t box2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {box0, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = fn(map, dtype, 3, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace sg
+
+using namespace sg;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool strides_ok(const sage_strides &s) {
+  return s.b >= 0 && s.h >= 0 && s.n >= 0 && (s.b % 8) == 0 && (s.h % 8) == 0 && (s.n % 8) == 0;
+}
+
+bool sizes_ok(int B, int H, int N) {
+  return B >= 1 && H >= 1 && N >= 1 && int64_t(B) * H <= 65535 && N <= (1 << 28);
+}
+
+sage_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
+
+float default_scale(float sm_scale) { return sm_scale > 0.f ? sm_scale : float(1.0 / std::sqrt(128.0)); }
+
+}  // namespace
+
+extern "C" {
+
+const char *sage_status_string(sage_status s) {
+  switch (s) {
+    case SAGE_OK: return "ok";
+    case SAGE_ERR_INVALID_ARG: return "invalid argument";
+    case SAGE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SAGE_ERR_CUDA: return "CUDA error";
+    case SAGE_ERR_WORKSPACE: return "workspace too small";
+    case SAGE_ERR_TIMEOUT: return "bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int sage_abi_version(void) { return kAbiVersion; }
+
+size_t sage_quantize_qk_workspace(int B, int H, int Nk) {
+  if (B < 1 || H < 1 || Nk < 1) return 0;
+  return size_t(B) * H * ceil_div(Nk, kMeanChunk) * kD * sizeof(float) + 16;
+}
+
+sage_status sage_quantize_qk(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks, int B,
+                             int H, int Nq, int Nk, int d, int q_block, int k_block, int8_t *q_codes,
+                             float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(k_bf16) || !aligned16(q_codes) || !aligned16(k_codes) ||
+      !aligned16(k_mean) || q_scales == nullptr || k_scales == nullptr || !aligned16(workspace))
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(qs) || !strides_ok(ks)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < sage_quantize_qk_workspace(B, H, Nk)) return SAGE_ERR_WORKSPACE;
+  return from_cuda(launch_quantize_qk(q_bf16, qs, k_bf16, ks, B, H, Nq, Nk, q_block, k_block, q_codes, q_scales,
+                                      k_codes, k_scales, k_mean, static_cast<float *>(workspace),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t sage_quantize_v_workspace(int B, int H, int Nk) {
+  if (B < 1 || H < 1 || Nk < 1) return 0;
+  return (size_t(B) * H * ceil_div(Nk, kMeanChunk) * kD + size_t(B) * H * kD) * sizeof(float) + 16;
+}
+
+sage_status sage_quantize_v(const void *v_bf16, sage_strides vs, int B, int H, int Nk, int d, uint8_t *v_codes,
+                            float *v_scales, void *workspace, size_t workspace_bytes, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if (!sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(v_bf16) || !aligned16(v_codes) || !aligned16(v_scales) || !aligned16(workspace))
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(vs)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < sage_quantize_v_workspace(B, H, Nk)) return SAGE_ERR_WORKSPACE;
+  float *partial = static_cast<float *>(workspace);
+  float *inv = partial + size_t(B) * H * ceil_div(Nk, kMeanChunk) * kD;
+  return from_cuda(
+      launch_quantize_v(v_bf16, vs, B, H, Nk, v_codes, v_scales, partial, inv, static_cast<cudaStream_t>(stream)));
+}
+
+size_t sage_attn_fwd_workspace(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+  return dense_workspace_bytes(B, H, Nq, Nk);
+}
+
+sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                          const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
+                          int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
+                          sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                          void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || q_scales == nullptr ||
+      k_scales == nullptr || v_scales == nullptr || !aligned16(out_bf16) || !aligned16(workspace))
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(os)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < sage_attn_fwd_workspace(B, H, Nq, Nk)) return SAGE_ERR_WORKSPACE;
+  DenseArgs a;
+  a.q_codes = q_codes;
+  a.q_scales = q_scales;
+  a.k_codes = k_codes;
+  a.k_scales = k_scales;
+  a.v_codes = v_codes;
+  a.v_scales = v_scales;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.q_block = q_block;
+  a.k_block = k_block;
+  a.sm_scale = default_scale(sm_scale);
+  a.out = out_bf16;
+  a.os = os;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.q_img = ws;
+  a.k_img = ws + size_t(B) * H * Nq * kD * 2;
+  a.status = status_dev;
+  return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t int8kv_prompt_attn_workspace(int Nq, int Hq, int Hkv, int Nk) {
+  if (Nq < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return 0;
+  return int8kv_workspace_bytes(Nq, Hq, Hkv, Nk);
+}
+
+sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
+                               const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
+                               const void *v_scale_f16, int64_t kv_head_stride, int64_t scale_head_stride, int Nq,
+                               int q_pos0, int Nk, int Hq, int Hkv, int d, float sm_scale, void *out_bf16,
+                               int64_t o_tok_stride, int64_t o_head_stride, void *workspace,
+                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if (Nq < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || q_pos0 < 0 || int64_t(q_pos0) + Nq > Nk) return SAGE_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return SAGE_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128 || Hkv > 65535 || Nk > (1 << 28)) return SAGE_ERR_UNSUPPORTED;
+  if (!aligned16(q_bf16) || !aligned16(k_cache) || !aligned16(v_cache) || k_scale_f16 == nullptr ||
+      v_scale_f16 == nullptr || !aligned16(out_bf16) || workspace == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  if (q_tok_stride < 0 || q_head_stride < 0 || (q_tok_stride % 8) || (q_head_stride % 8)) return SAGE_ERR_INVALID_ARG;
+  if (o_tok_stride < 0 || o_head_stride < 0 || (o_tok_stride % 4) || (o_head_stride % 4)) return SAGE_ERR_INVALID_ARG;
+  if (kv_head_stride < int64_t(Nk) * kD || (kv_head_stride % 16) || scale_head_stride < Nk)
+    return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < int8kv_prompt_attn_workspace(Nq, Hq, Hkv, Nk)) return SAGE_ERR_WORKSPACE;
+  Int8KVArgs a;
+  a.q = q_bf16;
+  a.q_tok = q_tok_stride;
+  a.q_head = q_head_stride;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale_f16;
+  a.v_scale = v_scale_f16;
+  a.kv_head_stride = kv_head_stride;
+  a.scale_head_stride = scale_head_stride;
+  a.Nq = Nq;
+  a.q_pos0 = q_pos0;
+  a.Nk = Nk;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.sm_scale = default_scale(sm_scale);
+  a.out = out_bf16;
+  a.o_tok = o_tok_stride;
+  a.o_head = o_head_stride;
+  a.workspace = workspace;
+  a.status = status_dev;
+  return from_cuda(launch_int8kv(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,581 @@
+// Causal prompt attention over an int8 KV cache with per-token fp16 scales,
+// grouped-query heads, for sm_103a.
+//
+// Pages: "Strata PR #2092" (v2 int8 prompt attention: a chunk of new queries
+// attends to the int8 KV cache; K/V staged per chunk together with their
+// scales; error reported against FP64) and "Strata PR #2146" (the same kernel,
+// one stage).
+//
+// GB300 design:
+//  * One 128-row tile holds QT = floor(128 / G) queries x the G query heads of
+//    one kv head (G = Hq / Hkv), so each K/V tile read serves all G heads.
+//  * S = Q.K^T on tcgen05 kind::f16 (bf16 queries x exact bf16 images of the
+//    int8 K codes), fp32 in TMEM.
+//  * softmax per row in fp32: s = S * fl(ks * sm_scale * log2 e), causal mask
+//    by absolute position, p = 2^(s - m).
+//  * P.V: the weight w = p * vs (scaled by a power of two so that w < 2) is
+//    split into fp16 hi + lo parts and multiplied with exact fp16 images of the
+//    V codes by one K = 256 kind::f16 MMA chain ([hi | lo] . [V ; V]), so the
+//    fp16 rounding of w does not reach the output.
+//  * The key range of each query tile is split into `nsplit` contiguous pieces
+//    (split-KV) so the grid fills the SMs; a combine kernel merges the (m, l,
+//    O) partials of one row in split order.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace sg {
+namespace kv {
+
+constexpr int BM = 128, BN = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kQBytes = BM * kD * 2;
+constexpr uint32_t kKTile = BN * kD * 2;
+constexpr uint32_t kVBytes = kD * BN * 2;               // fp16 V^T image
+constexpr uint32_t kPBytes = BM * BN * 2;               // one fp16 P tile
+constexpr uint32_t kPBuf = 2 * kPBytes;                 // hi + lo
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kQBytes;
+constexpr uint32_t kOffV = kOffK + kKTile;
+constexpr uint32_t kOffP = kOffV + kVBytes;             // two buffers of (hi, lo)
+constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+
+constexpr uint32_t kIdescQK = make_idesc(kFmtF32, kFmtBF16, kFmtBF16, BM, BN);
+constexpr uint32_t kIdescPV = make_idesc(kFmtF32, kFmtF16, kFmtF16, BM, kD);
+
+struct Params {
+  int Nq, q_pos0, Nk, Hkv, G, QT, nsplit, Npad;
+  const float *kt, *vs;        // [Hkv][Npad] fl(ks*C), vs
+  const uint32_t *vmax_bits;   // max vs over the cache (fp32 bits)
+  float *part_o;               // [units][128][128]
+  float2 *part_ml;             // [units][128] (m, l)
+  int32_t *status;
+};
+
+struct Bars {
+  uint64_t q_full;
+  uint64_t k_full, k_empty;
+  uint64_t v_full, v_empty;
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void report(int32_t *status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int kv_tiles_for(const Params &p, int qtile) {
+  const int last_q = min((qtile + 1) * p.QT, p.Nq) - 1;
+  const int last_key = min(p.q_pos0 + last_q, p.Nk - 1);
+  return last_key / BN + 1;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    int8kv_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+  volatile int *abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = blockIdx.x, qtile = blockIdx.y, g = blockIdx.z;
+  const int unit = (g * gridDim.y + qtile) * p.nsplit + split;
+  const int i0 = qtile * p.QT;
+  const int tiles = kv_tiles_for(p, qtile);
+  const int tb = int((int64_t(tiles) * split) / p.nsplit);
+  const int te = int((int64_t(tiles) * (split + 1)) / p.nsplit);
+  const int T = te - tb;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->k_full, 1);
+    mbar_init(&bars->k_empty, 1);
+    mbar_init(&bars->v_full, 1);
+    mbar_init(&bars->v_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 4);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (T <= 0) {
+    // empty key range: record an empty partial for the combine
+    if (warp >= 4) {
+      const int r = (warp - 4) * 32 + lane;
+      p.part_ml[int64_t(unit) * BM + r] = make_float2(-INFINITY, 0.f);
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(&bars->q_full, uint32_t(p.QT * p.G) * 256u);
+      tma_load_3d(smem + kOffQ, &tmQ, &bars->q_full, 0, g * p.G, i0);
+      tma_load_3d(smem + kOffQ + kQBytes / 2, &tmQ, &bars->q_full, 64, g * p.G, i0);
+      auto load_k = [&](int j) -> bool {
+        if (j >= 1 && !mbar_wait(&bars->k_empty, (j - 1) & 1, abort)) return false;
+        const int key0 = (tb + j) * BN;
+        mbar_arrive_expect_tx(&bars->k_full, kKTile);
+        tma_load_3d(smem + kOffK, &tmK, &bars->k_full, 0, key0, g);
+        tma_load_3d(smem + kOffK + kKTile / 2, &tmK, &bars->k_full, 64, key0, g);
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        if (j >= 1 && !mbar_wait(&bars->v_empty, (j - 1) & 1, abort)) return false;
+        mbar_arrive_expect_tx(&bars->v_full, kVBytes);
+        const int key0 = (tb + j) * BN;
+        tma_load_3d(smem + kOffV, &tmV, &bars->v_full, key0, 0, g);
+        tma_load_3d(smem + kOffV + kVBytes / 2, &tmV, &bars->v_full, key0 + 64, 0, g);
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
+      }
+      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(smem + kOffQ);
+      auto issue_qk = [&](int j) -> bool {
+        if (!mbar_wait(&bars->k_full, j & 1, abort)) return false;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(smem + kOffK);
+        const uint32_t dS = tmem + ((j & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
+          umma_f16(dS, sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
+        }
+        tc_commit(&bars->s_full[j & 1]);
+        tc_commit(&bars->k_empty);
+        return true;
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0);
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) ok = issue_qk(j + 1);
+        if (!ok) break;
+        ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort) && mbar_wait(&bars->v_full, j & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sP = smem_u32(smem + kOffP + (j & 1) * kPBuf);
+        const uint32_t sV = smem_u32(smem + kOffV);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k) {
+            const uint32_t off = (k >> 2) * (kPBytes / 2) + (k & 3) * 32;
+            umma_f16(tmem + kColO, sdesc_sw128(sP + half * kPBytes + off), sdesc_sw128(sV + off), kIdescPV,
+                     (j > 0) || (half > 0) || (k > 0));
+          }
+        }
+        tc_commit(&bars->v_empty);
+        tc_commit(&bars->pv_done[j & 1]);
+      }
+      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
+    }
+  } else if (warp >= 4) {
+    const int r = (warp - 4) * 32 + lane;
+    const int il = r / p.G;
+    const int qi = i0 + il;
+    const bool valid = (il < p.QT) && (qi < p.Nq);
+    const int pos = p.q_pos0 + qi;  // keys 0..pos are visible
+    const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+    // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16
+    const float vmax = __uint_as_float(*p.vmax_bits);
+    const int E = vmax > 0.f ? int((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
+    const float wscale = __uint_as_float(uint32_t(127 - E) << 23);  // 2^-E
+    const float *kt_row = p.kt + int64_t(g) * p.Npad;
+    const float *vs_row = p.vs + int64_t(g) * p.Npad;
+    float m = -INFINITY, l = 0.f;
+    const uint32_t sw = r & 7;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+      ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sa = lane_base + ((j & 1) ? kColS1 : kColS0);
+      const int key0 = (tb + j) * BN;
+      const float *kt = kt_row + key0;
+      const float *vsc = vs_row + key0;
+      const int nvis = min(BN, pos - key0 + 1);  // visible keys of this tile (<= 0: none)
+      // pass 1: row maximum of s = S * kt over the visible keys
+      float mt = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t S[32];
+        tmem_ld32(sa + 32 * c, S);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + 32 * c + i));
+          const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float v = __fmul_rn(__uint_as_float(S[i + u]), kk[u]);
+            if (32 * c + i + u < nvis) mt = fmaxf(mt, v);
+          }
+        }
+      }
+      const float mnew = fmaxf(m, mt);
+      const float alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
+      const float msub = (mnew == -INFINITY) ? 0.f : mnew;
+      // P buffer j&1 was last read by PV_{j-2}
+      if (j >= 2) {
+        ok = mbar_wait(&bars->pv_done[j & 1], ((j >> 1) + 1) & 1, abort);
+        if (!ok) break;
+      }
+      // pass 2: p = 2^(s - m'), row sum, w = p * vs * 2^-E split into fp16
+      // hi + lo and written to the swizzled P tiles (hi at +0, lo at +kPBytes;
+      // each tile is two 64-key column blocks of 128-byte rows)
+      float rowsum = 0.f;
+      uint8_t *dstP = smem + kOffP + (j & 1) * kPBuf + r * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t S[32];
+        tmem_ld32(sa + 32 * c, S);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int u4 = 0; u4 < 8; u4 += 4) {
+            const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + 32 * c + i + u4));
+            const float4 v4 = __ldg(reinterpret_cast<const float4 *>(vsc + 32 * c + i + u4));
+            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
+            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float v = __fmul_rn(__uint_as_float(S[i + u4 + u]), kk[u]);
+              if (32 * c + i + u4 + u >= nvis) v = -INFINITY;
+              const float pe = ex2(__fsub_rn(v, msub));
+              rowsum = __fadd_rn(rowsum, pe);
+              w[u] = __fmul_rn(pe, __fmul_rn(vv[u], wscale));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const __half2 h = __floats2half2_rn(w[u], w[u + 1]);
+              const float2 hf = __half22float2(h);
+              const __half2 lw = __floats2half2_rn(__fsub_rn(w[u], hf.x), __fsub_rn(w[u + 1], hf.y));
+              hi[(u4 + u) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
+              lo[(u4 + u) >> 1] = *reinterpret_cast<const uint32_t *>(&lw);
+            }
+          }
+          const int key = 32 * c + i;          // first of the 8 keys of this 16-byte chunk
+          const int cb = key >> 6, ch = (key & 63) >> 3;
+          uint8_t *d = dstP + cb * (kPBytes / 2) + ((ch ^ sw) << 4);
+          *reinterpret_cast<uint4 *>(d) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(d + kPBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
+      // O is stable once PV_{j-1} is complete; rescale it when the max grew
+      if (j >= 1) {
+        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + kColO + 32 * c, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
+            tmem_st32(lane_base + kColO + 32 * c, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      m = mnew;
+    }
+    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    if (!ok) {
+      report(p.status, SAGE_ERR_TIMEOUT);
+    } else {
+      tc_fence_after();
+      float *dst = p.part_o + (int64_t(unit) * BM + r) * kD;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kColO + 32 * c, o);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4 *>(dst + 32 * c + 4 * u) =
+                make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        }
+      }
+      p.part_ml[int64_t(unit) * BM + r] = make_float2(m, l);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Prepare the cache for the tensor cores: bf16 images of the K codes
+// [Hkv][Npad][128], fp16 images of the V codes transposed [Hkv][128][Npad],
+// kt = fl(ks * C) and vs as fp32 [Hkv][Npad] (zero past Nk), and the maximum
+// of vs.  grid (Npad/128, Hkv), 256 threads.
+__global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restrict__ kc, const int8_t *__restrict__ vc,
+                                                          const __half *__restrict__ ks, const __half *__restrict__ vs,
+                                                          int64_t kv_hs, int64_t sc_hs, int Nk, int Npad, float C,
+                                                          __nv_bfloat16 *__restrict__ kimg, __half *__restrict__ vtimg,
+                                                          float *__restrict__ kt, float *__restrict__ vsf,
+                                                          uint32_t *__restrict__ vmax_bits) {
+  __shared__ __half vt[kD][BN + 8];
+  const int tile = blockIdx.x, g = blockIdx.y;
+  const int key0 = tile * BN;
+  const int8_t *ksrc = kc + g * kv_hs;
+  const int8_t *vsrc = vc + g * kv_hs;
+  // K: 128 keys x 128 codes -> bf16, 16 codes per thread-step
+#pragma unroll
+  for (int rep = 0; rep < 4; ++rep) {
+    const int e = threadIdx.x + 256 * rep;  // 1024 chunks of 16 codes
+    const int key = e >> 3, c16 = (e & 7) * 16;
+    const int gk = key0 + key;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (gk < Nk) w = *reinterpret_cast<const uint4 *>(ksrc + int64_t(gk) * kD + c16);
+    const int8_t *b = reinterpret_cast<const int8_t *>(&w);
+    uint32_t o[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const __nv_bfloat162 t = __floats2bfloat162_rn(float(b[2 * u]), float(b[2 * u + 1]));
+      o[u] = *reinterpret_cast<const uint32_t *>(&t);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(kimg + (int64_t(g) * Npad + gk) * kD + c16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  // V: transpose through shared memory
+#pragma unroll
+  for (int rep = 0; rep < 4; ++rep) {
+    const int e = threadIdx.x + 256 * rep;
+    const int key = e >> 3, c16 = (e & 7) * 16;
+    const int gk = key0 + key;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (gk < Nk) w = *reinterpret_cast<const uint4 *>(vsrc + int64_t(gk) * kD + c16);
+    const int8_t *b = reinterpret_cast<const int8_t *>(&w);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) vt[c16 + u][key] = __int2half_rn(b[u]);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int rep = 0; rep < 8; ++rep) {
+    const int e = threadIdx.x + 256 * rep;  // 2048 chunks of 8 keys
+    const int ch = e >> 4, k8 = (e & 15) * 8;
+    const uint4 val = *reinterpret_cast<const uint4 *>(&vt[ch][k8]);
+    *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + k8) = val;
+  }
+  if (threadIdx.x < BN) {
+    const int gk = key0 + threadIdx.x;
+    float ktv = 0.f, vsv = 0.f;
+    if (gk < Nk) {
+      ktv = __fmul_rn(__half2float(ks[g * sc_hs + gk]), C);
+      vsv = __half2float(vs[g * sc_hs + gk]);
+    }
+    kt[int64_t(g) * Npad + gk] = ktv;
+    vsf[int64_t(g) * Npad + gk] = vsv;
+    float mx = fabsf(vsv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) atomicMax(vmax_bits, __float_as_uint(mx));
+  }
+}
+
+__global__ void zero_word_kernel(uint32_t *w) { *w = 0u; }
+
+// Merge the split partials of each (query, head) row in split order and write
+// bf16 output.  One warp per row, 4 channels per lane.
+__global__ void __launch_bounds__(256) int8kv_combine_kernel(const float *__restrict__ part_o,
+                                                             const float2 *__restrict__ part_ml,
+                                                             const uint32_t *__restrict__ vmax_bits, int Nq, int Hq,
+                                                             int G, int QT, int nqt, int nsplit,
+                                                             __nv_bfloat16 *__restrict__ out, int64_t o_tok,
+                                                             int64_t o_head) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= Nq * Hq) return;
+  const int qi = gw / Hq, h = gw - qi * Hq;
+  const int g = h / G, hl = h - g * G;
+  const int qtile = qi / QT, r = (qi - qtile * QT) * G + hl;
+  const int64_t unit0 = (int64_t(g) * nqt + qtile) * nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[(unit0 + s) * BM + r].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 ml = part_ml[(unit0 + s) * BM + r];
+    if (ml.x == -INFINITY) continue;
+    const float wgt = ex2(__fsub_rn(ml.x, M));
+    L = __fadd_rn(L, __fmul_rn(wgt, ml.y));
+    const float4 o = *reinterpret_cast<const float4 *>(part_o + ((unit0 + s) * BM + r) * kD + 4 * lane);
+    acc.x = __fadd_rn(acc.x, __fmul_rn(wgt, o.x));
+    acc.y = __fadd_rn(acc.y, __fmul_rn(wgt, o.y));
+    acc.z = __fadd_rn(acc.z, __fmul_rn(wgt, o.z));
+    acc.w = __fadd_rn(acc.w, __fmul_rn(wgt, o.w));
+  }
+  const float vmax = __uint_as_float(*vmax_bits);
+  const int E = vmax > 0.f ? ((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
+  const float back = __uint_as_float(uint32_t(127 + E) << 23);  // 2^E
+  const float inv = __fdiv_rn(back, L);
+  const __nv_bfloat162 a = __floats2bfloat162_rn(__fmul_rn(acc.x, inv), __fmul_rn(acc.y, inv));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(acc.z, inv), __fmul_rn(acc.w, inv));
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t *>(&a);
+  packed.y = *reinterpret_cast<const uint32_t *>(&b);
+  *reinterpret_cast<uint2 *>(out + int64_t(qi) * o_tok + int64_t(h) * o_head + 4 * lane) = packed;
+}
+
+struct Layout {
+  int G, QT, nqt, nsplit, Npad;
+  size_t off_kimg, off_vt, off_kt, off_vs, off_vmax, off_po, off_pml, total;
+};
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+static Layout layout(int Nq, int Hq, int Hkv, int Nk, int sms) {
+  Layout L;
+  L.G = Hq / Hkv;
+  L.QT = BM / L.G;
+  L.nqt = ceil_div(Nq, L.QT);
+  L.Npad = nk_pad(Nk);
+  // split-KV: pick the split count that minimises waves x (tiles per unit + 2)
+  const int tiles = ceil_div(Nk, BN);
+  const int64_t base_units = int64_t(Hkv) * L.nqt;
+  double best = 1e300;
+  L.nsplit = 1;
+  for (int s = 1; s <= 16 && s <= tiles; ++s) {
+    const int64_t units = base_units * s;
+    const int64_t waves = (units + sms - 1) / sms;
+    const double cost = double(waves) * (double(tiles) / s + 2.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      L.nsplit = s;
+    }
+  }
+  const int64_t units = base_units * L.nsplit;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  };
+  L.off_kimg = take(size_t(Hkv) * L.Npad * kD * 2);
+  L.off_vt = take(size_t(Hkv) * L.Npad * kD * 2);
+  L.off_kt = take(size_t(Hkv) * L.Npad * 4);
+  L.off_vs = take(size_t(Hkv) * L.Npad * 4);
+  L.off_vmax = take(4);
+  L.off_po = take(size_t(units) * BM * kD * 4);
+  L.off_pml = take(size_t(units) * BM * 8);
+  L.total = off + 256;
+  return L;
+}
+
+}  // namespace kv
+
+size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk) {
+  return kv::layout(Nq, Hq, Hkv, Nk, kv::sm_count()).total;
+}
+
+cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
+  using namespace kv;
+  const Layout L = layout(a.Nq, a.Hq, a.Hkv, a.Nk, sm_count());
+  uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255));
+  auto *kimg = reinterpret_cast<__nv_bfloat16 *>(ws + L.off_kimg);
+  auto *vtimg = reinterpret_cast<__half *>(ws + L.off_vt);
+  auto *kt = reinterpret_cast<float *>(ws + L.off_kt);
+  auto *vsf = reinterpret_cast<float *>(ws + L.off_vs);
+  auto *vmax = reinterpret_cast<uint32_t *>(ws + L.off_vmax);
+  auto *po = reinterpret_cast<float *>(ws + L.off_po);
+  auto *pml = reinterpret_cast<float2 *>(ws + L.off_pml);
+  const float C = a.sm_scale * 1.44269504f;
+
+  zero_word_kernel<<<1, 1, 0, st>>>(vmax);
+  int8kv_prep_kernel<<<dim3(L.Npad / BN, a.Hkv), 256, 0, st>>>(
+      a.k_cache, a.v_cache, static_cast<const __half *>(a.k_scale), static_cast<const __half *>(a.v_scale),
+      a.kv_head_stride, a.scale_head_stride, a.Nk, L.Npad, C, kimg, vtimg, kt, vsf, vmax);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tv;
+  if (!encode_tmap_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, a.Hq, a.Nq, uint64_t(a.q_head) * 2,
+                      uint64_t(a.q_tok) * 2, 64, L.G, L.QT) ||
+      !encode_tmap_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kimg, kD, L.Npad, a.Hkv, kD * 2,
+                      uint64_t(L.Npad) * kD * 2, 64, BN, 1) ||
+      !encode_tmap_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, vtimg, L.Npad, kD, a.Hkv, uint64_t(L.Npad) * 2,
+                      uint64_t(L.Npad) * kD * 2, 64, kD, 1))
+    return cudaErrorInvalidValue;
+
+  Params p;
+  p.Nq = a.Nq;
+  p.q_pos0 = a.q_pos0;
+  p.Nk = a.Nk;
+  p.Hkv = a.Hkv;
+  p.G = L.G;
+  p.QT = L.QT;
+  p.nsplit = L.nsplit;
+  p.Npad = L.Npad;
+  p.kt = kt;
+  p.vs = vsf;
+  p.vmax_bits = vmax;
+  p.part_o = po;
+  p.part_ml = pml;
+  p.status = a.status;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(int8kv_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int8kv_attn_kernel<<<dim3(L.nsplit, L.nqt, a.Hkv), kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int rows = a.Nq * a.Hq;
+  int8kv_combine_kernel<<<ceil_div(rows, 8), 256, 0, st>>>(po, pml, vmax, a.Nq, a.Hq, L.G, L.QT, L.nqt, L.nsplit,
+                                                          static_cast<__nv_bfloat16 *>(a.out), a.o_tok, a.o_head);
+  return cudaGetLastError();
+}
+
+}  // namespace sg

@@ -1,0 +1,67 @@
+// Internal launchers shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/sage_gb300.h"
+
+namespace sg {
+
+constexpr int kD = 128;          // head dimension
+constexpr int kMeanChunk = 256;  // tokens per K-mean partial sum
+constexpr int kTile = 128;       // keys per softmax tile
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int nk_pad(int nk) { return ceil_div(nk, kTile) * kTile; }
+
+// quantisers (quant.cu)
+cudaError_t launch_quantize_qk(const void *q, sage_strides qs, const void *k, sage_strides ks, int B, int H,
+                               int Nq, int Nk, int q_block, int k_block, int8_t *q_codes, float *q_scales,
+                               int8_t *k_codes, float *k_scales, float *k_mean, float *partial,
+                               cudaStream_t st);
+cudaError_t launch_quantize_v(const void *v, sage_strides vs, int B, int H, int Nk, uint8_t *v_codes,
+                              float *v_scales, float *partial, float *inv, cudaStream_t st);
+
+// dense attention (attn_dense.cu)
+struct DenseArgs {
+  const int8_t *q_codes;
+  const float *q_scales;
+  const int8_t *k_codes;
+  const float *k_scales;
+  const uint8_t *v_codes;
+  const float *v_scales;
+  int B, H, Nq, Nk, q_block, k_block;
+  float sm_scale;
+  void *out;
+  sage_strides os;
+  void *q_img, *k_img;  // workspace: fp16 images of the codes
+  int32_t *status;
+};
+size_t dense_workspace_bytes(int B, int H, int Nq, int Nk);
+cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st);
+
+// int8 KV-cache prompt attention (attn_int8kv.cu)
+struct Int8KVArgs {
+  const void *q;
+  int64_t q_tok, q_head;
+  const int8_t *k_cache, *v_cache;
+  const void *k_scale, *v_scale;
+  int64_t kv_head_stride, scale_head_stride;
+  int Nq, q_pos0, Nk, Hq, Hkv;
+  float sm_scale;
+  void *out;
+  int64_t o_tok, o_head;
+  void *workspace;
+  int32_t *status;
+};
+size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk);
+cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st);
+
+// tensor-map encoding through the driver entry point (api.cu)
+bool encode_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                    uint32_t box2);
+
+}  // namespace sg

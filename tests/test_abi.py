@@ -1,0 +1,112 @@
+"""The C-ABI library: it builds for sm_103a, loads, exports every function the
+header declares, and rejects bad arguments on the host before any launch.
+No compute call is made here (these tests run without a GPU)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import quantized_attention_sage_gb300 as qas
+from quantized_attention_sage_gb300 import Strides
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sage_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    qas.build()
+    return qas.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([a-z][a-z0-9_]*)\s*\(", text)
+    skip = {"sizeof", "if", "return"}
+    return sorted({n for n in names if n not in skip and (n.startswith("sage_") or n.startswith("int8kv_"))})
+
+
+def test_header_declares_the_four_entry_points():
+    names = declared_functions()
+    for n in ("sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd", "int8kv_prompt_attn"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version_and_status_strings(L):
+    assert L.sage_abi_version() == 1
+    assert L.sage_status_string(0) == b"ok"
+    assert L.sage_status_string(4) == b"workspace too small"
+    assert L.sage_status_string(99) == b"unknown status"
+
+
+def test_workspace_queries(L):
+    assert L.sage_quantize_qk_workspace(1, 24, 37810) >= 24 * 148 * 128 * 4
+    assert L.sage_quantize_v_workspace(1, 24, 37810) >= 24 * 149 * 128 * 4
+    assert L.sage_attn_fwd_workspace(1, 24, 37810, 37810) >= 2 * 24 * 37810 * 128 * 2
+    assert L.int8kv_prompt_attn_workspace(1024, 32, 8, 32768) > 2 * 8 * 32768 * 128 * 2
+    assert L.sage_quantize_qk_workspace(0, 1, 1) == 0
+    assert L.int8kv_prompt_attn_workspace(4, 6, 4, 10) == 0  # Hq % Hkv != 0
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def s4(b, h, n):
+    return Strides(b, h, n)
+
+
+def test_quantize_qk_rejects_bad_arguments(L):
+    st = s4(2 * 256 * 128, 256 * 128, 128)
+    ok_args = dict(q=FAKE, qs=st, k=FAKE, ks=st, B=1, H=2, Nq=256, Nk=256, d=128, qb=64, kb=64)
+
+    def call(**kw):
+        a = dict(ok_args)
+        a.update(kw)
+        return L.sage_quantize_qk(a["q"], a["qs"], a["k"], a["ks"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                                  a["qb"], a["kb"], FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  a.get("wsb", 0), None)
+    assert call(d=64) == 2
+    assert call(qb=32) == 2
+    assert call(kb=256) == 2
+    assert call(Nq=0) == 1
+    assert call(B=0) == 1
+    assert call(q=None) == 1
+    assert call(k=FAKE + 8) == 1                       # misaligned
+    assert call(qs=s4(2 * 256 * 128, 256 * 128, 100)) == 1  # stride not a multiple of 8
+    assert call(wsb=0) == 4                            # workspace too small
+
+
+def test_quantize_v_and_attn_reject_bad_arguments(L):
+    st = s4(2 * 256 * 128, 256 * 128, 128)
+    assert L.sage_quantize_v(FAKE, st, 1, 2, 256, 100, FAKE, FAKE, FAKE, 1 << 30, None) == 2
+    assert L.sage_quantize_v(None, st, 1, 2, 256, 128, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert L.sage_quantize_v(FAKE, st, 1, 2, 256, 128, FAKE, FAKE, FAKE, 0, None) == 4
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 64, 48, 0.0, FAKE, st,
+                           FAKE, 1 << 30, None, None) == 2
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 64, 64, 0.0, None, st,
+                           FAKE, 1 << 30, None, None) == 1
+    assert L.sage_attn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 64, 64, 0.0, FAKE, st,
+                           FAKE, 16, None, None) == 4
+
+
+def test_int8kv_rejects_bad_arguments(L):
+    def call(Nq=8, q_pos0=8, Nk=16, Hq=4, Hkv=2, d=128, kvhs=16 * 128, q=FAKE, wsb=1 << 30):
+        return L.int8kv_prompt_attn(q, Hq * 128, 128, FAKE, FAKE, FAKE, FAKE, kvhs, Nk, Nq, q_pos0, Nk, Hq,
+                                    Hkv, d, 0.0, FAKE, Hq * 128, 128, FAKE, wsb, None, None)
+    assert call(d=96) == 2
+    assert call(Hq=6, Hkv=4) == 1        # not a whole number of query heads per kv head
+    assert call(q_pos0=9) == 1           # q_pos0 + Nq > Nk
+    assert call(q_pos0=-1) == 1
+    assert call(kvhs=100) == 1           # kv head stride below Nk * 128
+    assert call(q=FAKE + 4) == 1
+    assert call(wsb=0) == 4
