@@ -1,0 +1,404 @@
+"""Benchmark of the GB300 quantized attention path.
+
+One step = the whole dense path over the 37,810-token, 24-head video-DiT
+self-attention workload (B=1, H=24, Nq=Nk=37,810, d=128, Q/K INT8 per
+128-token blocks, FP8 V): sage_quantize_qk + sage_quantize_v + sage_attn_fwd,
+inputs already resident in HBM.  The metric is effective TFLOP/s
+(4 * Nq * Nk * d * H per step); ms per step is reported beside it.
+
+Also measured in the same run (JSON keys, not extra lines):
+  * per-call times of the three dense entry points (CUDA events around each
+    call inside the timed steps) and the roofline of the attention call;
+  * int8kv_prompt_attn on the 32K x 1024 and 64K x 512 int8 KV-cache chunks;
+  * e2e: the same step through the public API with pinned host buffers
+    (host->device copy of Q, K, V and device->host copy of the output inside
+    the timed region);
+  * cpu_baseline: the CPU oracle on a bounded sample of the workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun every rank runs the full workload on its own GPU (heads of
+independent problems, no collective on the data path: weak scaling); rank 0
+prints the line with the maximum time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "quantized attention fwd effective TFLOPS (4*Nq*Nk*d*H), video-DiT 37,810-token self-attention"
+UNIT = "TFLOP/s"
+WORKLOAD = "videodit_b1h24n37810"
+
+# dram bytes (read + write) per launch of the attention call, from one ncu
+# capture of the kernel source with this sha256 prefix; None when the source
+# has changed since.
+TRAFFIC = {"sha256_prefix": None, "bytes": None}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_sha(name: str) -> str:
+    p = os.path.join(ROOT, "quantized_attention_sage_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(parts)
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * max(power)] if power else sm
+        return {"sm_mhz": statistics.median(loaded or sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(target_s: float = 12.0):
+    """Time the oracle on one head of the workload: its quantisation and the
+    attention of a sample of query rows, scaled to the whole workload."""
+    import oracle
+
+    w = synth.dense_workload(WORKLOAD)
+    x = synth.dense_inputs(w, heads=(0, 1))
+    q, k, v = x["q"][0, 0], x["k"][0, 0], x["v"][0, 0]
+    t0 = time.perf_counter()
+    mu = oracle.k_mean(k)
+    qc, sq = oracle.quant_q(q, w.block)
+    kc, sk = oracle.quant_k(k, w.block, mu)
+    vct, sv = oracle.quant_v(v)
+    t_quant = time.perf_counter() - t0
+    rng = np.random.default_rng(3)
+    rows_done, t_rows, threads = 0, 0.0, 1
+    batch = 32
+    while t_rows < target_s and rows_done < w.Nq:
+        rows = rng.integers(0, w.Nq, batch).astype(np.int32)
+        t1 = time.perf_counter()
+        _, _, threads = oracle.sage_attn_rows(qc, sq, w.block, kc, sk, w.block, vct, sv, w.Nq, w.Nk, rows=rows)
+        t_rows += time.perf_counter() - t1
+        rows_done += batch
+        if t_rows > 0 and rows_done == batch:
+            batch = max(batch, int(batch * (target_s / 2) / t_rows))
+    per_row = t_rows / rows_done
+    est_s = w.B * w.H * (t_quant + per_row * w.Nq)
+    return {"value": w.flops / est_s / 1e12, "unit": UNIT, "cores": int(threads), "kind": "oracle",
+            "sample": (f"head 0 of {WORKLOAD}: quantisation of the head ({t_quant:.2f} s) and the "
+                       f"attention of {rows_done} random query rows ({t_rows:.2f} s), scaled to "
+                       f"24 heads x 37,810 rows"),
+            "seconds": t_quant + t_rows, "est_full_seconds": est_s}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    per_step = max(2.0, min(15.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(per_step / 4)
+    vals, secs = [], []
+    last = None
+    for _ in range(args.steps):
+        last = oracle_sample(per_step)
+        vals.append(last["value"])
+        secs.append(last["est_full_seconds"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, the workload's shapes)",
+        "config": {"workload": WORKLOAD, "B": 1, "H": 24, "Nq": 37810, "Nk": 37810, "d": 128, "block": 128,
+                   "note": "CPU oracle (plain C, OpenMP) on a bounded sample, scaled to the workload"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+
+    import quantized_attention_sage_gb300 as qas
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    qas.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    w = synth.dense_workload(WORKLOAD)
+    x = synth.dense_inputs(w)
+
+    def to_pinned(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = to_pinned(x["q"]), to_pinned(x["k"]), to_pinned(x["v"])
+    q, k, v = hq.to(dev), hk.to(dev), hv.to(dev)
+    B, H, N, D = q.shape
+    bq = bk = w.block
+    nb = -(-N // bq)
+    qk = dict(q_codes=torch.empty((B, H, N, D), dtype=torch.int8, device=dev),
+              q_scales=torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+              k_codes=torch.empty((B, H, N, D), dtype=torch.int8, device=dev),
+              k_scales=torch.empty((B, H, nb), dtype=torch.float32, device=dev),
+              k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev))
+    vq = dict(v_codes=torch.empty((B, H, D, qas.nk_pad(N)), dtype=torch.uint8, device=dev),
+              v_scales=torch.empty((B, H, D), dtype=torch.float32, device=dev))
+    out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=dev)
+    L = qas.lib()
+    ws_qk = torch.empty(L.sage_quantize_qk_workspace(B, H, N), dtype=torch.uint8, device=dev)
+    ws_v = torch.empty(L.sage_quantize_v_workspace(B, H, N), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(L.sage_attn_fwd_workspace(B, H, N, N), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        qas.sage_quantize_qk(q, k, bq, bk, out=qk, workspace=ws_qk)
+        if ev is not None:
+            ev[1].record(stream)
+        qas.sage_quantize_v(v, out=vq, workspace=ws_v)
+        if ev is not None:
+            ev[2].record(stream)
+        qas.sage_attn_fwd(qk, vq, bq, bk, out=out, workspace=ws_a, status=status)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert status.item() == 0, "device status set during warm-up"
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    assert status.item() == 0, "device status set during the timed steps"
+    ms_step = ms_total / args.steps
+    comp = {
+        "sage_quantize_qk_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+        "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+        "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+    }
+    value = world * w.flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    hout = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(2, min(args.steps, 5))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e = {"value": world * w.flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+           "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
+
+    # ---- int8 KV-cache prompt attention
+    kv = {}
+    for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
+        wk = synth.int8kv_workload(name)
+        y = synth.int8kv_inputs(wk)
+        tq = torch.from_numpy(y["q"].view(np.int16)).view(torch.bfloat16).to(dev)
+        kc = torch.from_numpy(y["k"]).to(dev)
+        vc = torch.from_numpy(y["v"]).to(dev)
+        ks = torch.from_numpy(y["k_scale"]).to(dev)
+        vs = torch.from_numpy(y["v_scale"]).to(dev)
+        o = torch.empty((wk.Nq, wk.Hq, 128), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(L.int8kv_prompt_attn_workspace(wk.Nq, wk.Hq, wk.Hkv, wk.Nk), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0, out=o, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        reps = max(5, args.steps)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0, out=o, workspace=ws, status=status)
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        kv[name] = {"ms": ms, "tflops_formula": wk.flops / (ms * 1e-3) / 1e12,
+                    "tflops_causal": 4 * wk.visible_pairs * 128 * wk.Hq / (ms * 1e-3) / 1e12,
+                    "Nq": wk.Nq, "Nk": wk.Nk, "Hq": wk.Hq, "Hkv": wk.Hkv}
+    assert status.item() == 0, "device status set in int8kv_prompt_attn"
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks()
+    p16 = pk["bf16_tflops"]
+    # Q.K^T on the f16 tensor path, P.V on FP8 (2x the f16 rate, nominal ratio):
+    # equal FLOPs on both, so the effective peak is the harmonic combination.
+    peak_mixed = 2.0 / (1.0 / p16 + 1.0 / (2.0 * p16))
+    achieved = w.flops / (comp["sage_attn_fwd_ms"] * 1e-3) / 1e12
+    sha = kernel_sha("attn_dense.cu")[:16]
+    traffic = TRAFFIC["bytes"] if TRAFFIC["sha256_prefix"] == sha else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8/fp8 (fp32 accumulate)",
+        "data": "synthetic (seeded SplitMix64/Box-Muller, the workload's shapes)",
+        "config": {"workload": WORKLOAD, "B": 1, "H": 24, "Nq": 37810, "Nk": 37810, "d": 128, "q_block": 128,
+                   "k_block": 128, "causal": False, "l2": "inputs larger than L2 (696 MB of Q/K/V)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "sage_attn_fwd (int8->fp16 image pass + tcgen05 attention kernel)",
+                     "bound": "tensor", "achieved": achieved, "peak": peak_mixed, "unit": "TFLOP/s",
+                     "frac": achieved / peak_mixed, "traffic": traffic,
+                     "peak_note": (f"{pk['source']}: bf16 burst {p16} TFLOP/s for the Q.K^T half, x2 (nominal "
+                                   f"fp8/bf16 ratio) for the P.V half")},
+        "components": comp,
+        "int8kv": kv,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 9 * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        cb = oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()
