@@ -383,6 +383,41 @@ def run_ours(args, rank, world):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """A small workload for profiler captures: a few calls of one path."""
+    import torch
+
+    import quantized_attention_sage_gb300 as qas
+
+    qas.build()
+    torch.cuda.set_device(0)
+    if args.case == "dense":
+        w = synth.DenseWorkload("profile_case", 11, 1, args.heads, args.seq, args.seq, 128)
+        x = synth.dense_inputs(w)
+        q, k, v = (torch.from_numpy(x[t].view(np.int16)).view(torch.bfloat16).cuda() for t in ("q", "k", "v"))
+        run = lambda: qas.sage_attention(q, k, v, 128, 128)  # noqa: E731
+        flops = w.flops
+    else:
+        wk = synth.Int8KVWorkload("profile_case", 12, args.queries, args.seq, args.heads, max(1, args.heads // 4))
+        y = synth.int8kv_inputs(wk)
+        tq = torch.from_numpy(y["q"].view(np.int16)).view(torch.bfloat16).cuda()
+        kc, vc = torch.from_numpy(y["k"]).cuda(), torch.from_numpy(y["v"]).cuda()
+        ks, vs = torch.from_numpy(y["k_scale"]).cuda(), torch.from_numpy(y["v_scale"]).cuda()
+        run = lambda: qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0)  # noqa: E731
+        flops = wk.flops
+    for _ in range(args.reps):
+        run()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    run()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    print(json.dumps({"case": args.case, "heads": args.heads, "seq": args.seq, "ms": ms,
+                      "tflops": flops / (ms * 1e-3) / 1e12}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -391,7 +426,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--case", choices=["dense", "int8kv"], default=None,
+                    help="run a small workload of one path (profiler captures) instead of the bench")
+    ap.add_argument("--heads", type=int, default=24)
+    ap.add_argument("--seq", type=int, default=8192)
+    ap.add_argument("--queries", type=int, default=1024)
+    ap.add_argument("--reps", type=int, default=2)
     args = ap.parse_args()
+    if args.case:
+        run_case(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
