@@ -9,7 +9,8 @@
  *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
  *    allocates no device memory and never synchronises the stream.  Scratch
  *    memory, where an entry point needs some, is passed in by the caller; its
- *    size comes from the matching *_workspace() query.
+ *    size comes from the matching *_workspace() query.  The one exception,
+ *    sage_quantize_qk_noalloc, uses a fixed scratch array held by the library.
  *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
  *    default stream).  Work is enqueued asynchronously.
  *  - Argument errors are detected on the host before anything is launched and
@@ -23,8 +24,9 @@
  *  - Head dimension d must be 128.  Element strides describe [B, H, N, d]
  *    tensors whose channel stride is 1; every stride and base pointer must be
  *    16-byte aligned (strides are multiples of 8 elements for bf16).
- *  - Inputs must be finite.  The functions hold no global state and may be
- *    called from several host threads.
+ *  - Inputs must be finite.  The functions hold no global state (except the
+ *    scratch array of sage_quantize_qk_noalloc) and may be called from several
+ *    host threads.
  *
  * Citations name the page and its section that defines each operation.
  */
@@ -45,6 +47,7 @@ typedef int sage_status;
 #define SAGE_ERR_CUDA 3         /* a CUDA call or kernel launch failed            */
 #define SAGE_ERR_WORKSPACE 4    /* workspace smaller than the *_workspace() size  */
 #define SAGE_ERR_TIMEOUT 5      /* device side: a bounded wait ran out            */
+#define SAGE_ERR_TOO_LARGE 6    /* beyond the fixed scratch of sage_quantize_qk_noalloc */
 
 /* Element strides of a [B, H, N, 128] tensor (channel stride is 1). */
 typedef struct {
@@ -87,6 +90,36 @@ sage_status sage_quantize_qk(const void *q_bf16, sage_strides qs, const void *k_
                              int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
                              int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
                              float *k_mean, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sage_quantize_qk_noalloc - the same computation and outputs as
+ * sage_quantize_qk, for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that must not allocate: a serving engine that reserves all of HBM at start
+ * and hands out fixed buffers, a plug-in whose host framework owns every
+ * device allocation, or a latency-bound loop where a cudaMalloc (which may
+ * synchronise the device) is not allowed.  Such a caller still passes its
+ * inputs and outputs; only the scratch is taken care of here.
+ *
+ * Scratch: a static device array of SAGE_QK_NOALLOC_SCRATCH_BYTES (8 MiB)
+ * inside the library, held by every GPU that loads the library until the
+ * process exits.  It holds the K-mean chunk partials, B*H*ceil(Nk/256)*128
+ * fp32 values, so B*H*ceil(Nk/256) <= 16384 (for example 24 heads up to
+ * 174,848 keys); larger problems return SAGE_ERR_TOO_LARGE and launch nothing.
+ * Each call writes every partial it later reads, so nothing needs clearing
+ * between calls.  All calls on a device share the one array: calls whose
+ * kernels overlap on the GPU (different streams, or different host threads)
+ * race on it and must be serialised by the caller.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Allocates nothing: no cudaMalloc or cudaFree.
+ * ---------------------------------------------------------------------- */
+#define SAGE_QK_NOALLOC_SCRATCH_BYTES (8u << 20)
+sage_status sage_quantize_qk_noalloc(const void *q_bf16, sage_strides qs, const void *k_bf16,
+                                     sage_strides ks, int B, int H, int Nq, int Nk, int d, int q_block,
+                                     int k_block, int8_t *q_codes, float *q_scales, int8_t *k_codes,
+                                     float *k_scales, float *k_mean, void *stream);
 
 /* ------------------------------------------------------------------------
  * sage_quantize_v - FP8 E4M3 per-channel quantisation of V, written

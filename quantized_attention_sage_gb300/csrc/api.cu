@@ -76,6 +76,7 @@ const char *sage_status_string(sage_status s) {
     case SAGE_ERR_CUDA: return "CUDA error";
     case SAGE_ERR_WORKSPACE: return "workspace too small";
     case SAGE_ERR_TIMEOUT: return "bounded device wait timed out";
+    case SAGE_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }
@@ -102,6 +103,23 @@ sage_status sage_quantize_qk(const void *q_bf16, sage_strides qs, const void *k_
   return from_cuda(launch_quantize_qk(q_bf16, qs, k_bf16, ks, B, H, Nq, Nk, q_block, k_block, q_codes, q_scales,
                                       k_codes, k_scales, k_mean, static_cast<float *>(workspace),
                                       static_cast<cudaStream_t>(stream)));
+}
+
+sage_status sage_quantize_qk_noalloc(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                                     int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
+                                     int8_t *q_codes, float *q_scales, int8_t *k_codes, float *k_scales,
+                                     float *k_mean, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(k_bf16) || !aligned16(q_codes) || !aligned16(k_codes) ||
+      !aligned16(k_mean) || q_scales == nullptr || k_scales == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(qs) || !strides_ok(ks)) return SAGE_ERR_INVALID_ARG;
+  if (sage_quantize_qk_workspace(B, H, Nk) - 16 > kNoAllocScratchBytes) return SAGE_ERR_TOO_LARGE;
+  return from_cuda(launch_quantize_qk_noalloc(q_bf16, qs, k_bf16, ks, B, H, Nq, Nk, q_block, k_block, q_codes,
+                                              q_scales, k_codes, k_scales, k_mean,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 size_t sage_quantize_v_workspace(int B, int H, int Nk) {

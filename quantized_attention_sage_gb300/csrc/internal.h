@@ -21,6 +21,12 @@ cudaError_t launch_quantize_qk(const void *q, sage_strides qs, const void *k, sa
                                int Nq, int Nk, int q_block, int k_block, int8_t *q_codes, float *q_scales,
                                int8_t *k_codes, float *k_scales, float *k_mean, float *partial,
                                cudaStream_t st);
+// allocation-free variant: scratch in a static device array of this size
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+cudaError_t launch_quantize_qk_noalloc(const void *q, sage_strides qs, const void *k, sage_strides ks, int B,
+                                       int H, int Nq, int Nk, int q_block, int k_block, int8_t *q_codes,
+                                       float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean,
+                                       cudaStream_t st);
 cudaError_t launch_quantize_v(const void *v, sage_strides vs, int B, int H, int Nk, uint8_t *v_codes,
                               float *v_scales, float *partial, float *inv, cudaStream_t st);
 

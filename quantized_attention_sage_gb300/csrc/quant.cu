@@ -10,6 +10,8 @@
 // the codes are bit-identical to the fp32 program they implement.
 #include <cuda_bf16.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -287,6 +289,47 @@ cudaError_t launch_quantize_v(const void *v, sage_strides vs, int B, int H, int 
   const int npad = nk_pad(Nk);
   v_encode_kernel<<<dim3(npad / kTile, B * H), 256, 0, st>>>(vv, vs, H, Nk, npad, inv, v_codes);
   return cudaGetLastError();
+}
+
+// -------------------------------------------------------------------------
+// Allocation-free variant of sage_quantize_qk.  Its K-mean chunk partials
+// live in this fixed device array instead of a caller workspace; every GPU
+// that loads the library holds it until the process exits.
+// -------------------------------------------------------------------------
+static __device__ __align__(256) float g_qk_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_qk_scratch on the current device, looked up once per
+// device (cudaGetSymbolAddress with that device current).  In host code the
+// array's name is only a host-side stand-in, never a device address.
+static cudaError_t noalloc_scratch(float **out) {
+  static std::mutex mu;
+  static float *ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (ptrs[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_qk_scratch);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = static_cast<float *>(p);
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_quantize_qk_noalloc(const void *q, sage_strides qs, const void *k, sage_strides ks, int B,
+                                       int H, int Nq, int Nk, int q_block, int k_block, int8_t *q_codes,
+                                       float *q_scales, int8_t *k_codes, float *k_scales, float *k_mean,
+                                       cudaStream_t st) {
+  float *scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return e;
+  return launch_quantize_qk(q, qs, k, ks, B, H, Nq, Nk, q_block, k_block, q_codes, q_scales, k_codes, k_scales,
+                            k_mean, scratch, st);
 }
 
 }  // namespace sg
