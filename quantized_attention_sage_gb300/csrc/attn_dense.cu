@@ -14,9 +14,24 @@
 //    TMEM).
 //  * Q, K (fp16 images) and V^T (E4M3) tiles arrive by TMA into 128-byte
 //    swizzled shared memory; S (double-buffered) and O live in TMEM.
-//  * Warp roles: warp 0 issues TMA, warp 1 issues MMAs and owns TMEM, warps
-//    4-7 own one query row per thread (TMEM lane = row): softmax, the O
-//    rescale in TMEM when the row maximum grows, and the epilogue.
+//  * One CTA owns two 128-row query tiles of one (b, h); every K/V tile read
+//    serves both.  Warp 0 issues TMA, warp 1 issues MMAs and owns TMEM,
+//    warps 4-7 and 8-11 are two softmax warpgroups, one per query tile, one
+//    query row per thread (TMEM lane = row).  TMEM: S0, S1, O0, O1, 128
+//    columns each.
+//  * P_t (E4M3) is written by the softmax into TMEM over the first 32 columns
+//    of S_t, whose scores are already in registers; the P.V MMA reads its A
+//    operand from TMEM.
+//  * MMA issue order per KV tile j: PV_t(j) then QK_t(j+1), alternating the
+//    two tiles, so while one warpgroup runs the softmax of its tile the tensor
+//    core works on the other tile (ping-pong).  tcgen05 MMAs issued by one
+//    thread execute in order, so QK_t(j+1) overwrites S_t/P_t only after
+//    PV_t(j) has read P_t, and "S_t(j+1) is ready" implies "PV_t(j) is
+//    complete": the softmax rescales O_t and writes P_t without another wait.
+//  * Softmax per element: row max on the raw int32-valued S (the dequant
+//    multiplier is positive, so max(fl(S*t)) = fl(max(S)*t)), one FFMA for
+//    S*t - m' + log2(448), ex2 on MUFU (448*p directly), fp32 row sums of
+//    448*p, E4M3 conversion of 448*p.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -26,23 +41,24 @@
 namespace sg {
 namespace dense {
 
-constexpr int BM = 128, BN = 128, NS = 3;
-constexpr int kThreads = 256;
-constexpr uint32_t kQBytes = BM * kD * 2;    // 32 KB fp16
+constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
+constexpr int kThreads = 384;
+constexpr uint32_t kQBytes = BM * kD * 2;    // 32 KB fp16 per query tile
 constexpr uint32_t kKBytes = BN * kD * 2;    // 32 KB fp16
 constexpr uint32_t kVBytes = kD * BN;        // 16 KB e4m3
-constexpr uint32_t kPBytes = BM * BN;        // 16 KB e4m3
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + NS * kKBytes;
-constexpr uint32_t kOffP = kOffV + NS * kVBytes;
-constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffQ = 0;                // two query tiles
+constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
+constexpr uint32_t kOffV = kOffK + NSK * kKBytes;
+constexpr uint32_t kOffBar = kOffV + NSV * kVBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+__host__ __device__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return t ? 384u : 256u; }
 
 constexpr uint32_t kIdescQK = make_idesc(kFmtF32, kFmtF16, kFmtF16, BM, BN);
 constexpr uint32_t kIdescPV = make_idesc(kFmtF32, kFmtE4M3, kFmtE4M3, BM, kD);
+constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
 struct Params {
   const float *q_scales, *k_scales, *v_scales;
@@ -55,9 +71,8 @@ struct Params {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[NS], k_empty[NS], v_full[NS], v_empty[NS];
-  uint64_t s_full[2], p_full[2];
-  uint64_t pv_done;
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -76,23 +91,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, bh = blockIdx.y;
-  const int q0 = qt * BM;
+  const int bh = blockIdx.y;
+  const int q0 = blockIdx.x * 2 * BM;
+  const int ntile = (q0 + BM < p.Nq) ? 2 : 1;  // second query tile present?
   const int T = ceil_div(p.Nk, BN);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 4);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->o_done[t], 1);
     }
-    mbar_init(&bars->pv_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -111,13 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      uint8_t *sQ = smem + kOffQ;
-      mbar_arrive_expect_tx(&bars->q_full, kQBytes);
-      tma_load_3d(sQ, &tmQ, &bars->q_full, 0, q0, bh);
-      tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0, bh);
+      mbar_arrive_expect_tx(&bars->q_full, ntile * kQBytes);
+      for (int t = 0; t < ntile; ++t) {
+        uint8_t *sQ = smem + kOffQ + t * kQBytes;
+        tma_load_3d(sQ, &tmQ, &bars->q_full, 0, q0 + t * BM, bh);
+        tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0 + t * BM, bh);
+      }
       auto load_k = [&](int j) -> bool {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(&bars->k_empty[s], ((j / NS) + 1) & 1, abort)) return false;
+        const int s = j % NSK;
+        if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
         uint8_t *dst = smem + kOffK + s * kKBytes;
         mbar_arrive_expect_tx(&bars->k_full[s], kKBytes);
         tma_load_3d(dst, &tmK, &bars->k_full[s], 0, j * BN, bh);
@@ -125,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto load_v = [&](int j) -> bool {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(&bars->v_empty[s], ((j / NS) + 1) & 1, abort)) return false;
+        const int s = j % NSV;
+        if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
         mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
         tma_load_3d(smem + kOffV + s * kVBytes, &tmV, &bars->v_full[s], j * BN, 0, bh);
         return true;
@@ -141,159 +161,191 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + kOffQ);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(&bars->k_full[s], (j / NS) & 1, abort)) return false;
-        tc_fence_after();
+      auto issue_qk = [&](int t, int s) {
+        const uint32_t sQ = smem_u32(smem + kOffQ + t * kQBytes);
         const uint32_t sK = smem_u32(smem + kOffK + s * kKBytes);
-        const uint32_t dS = tmem + ((j & 1) ? kColS1 : kColS0);
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
           const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
-          umma_f16(dS, sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
+          umma_f16(tmem + col_s(t), sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
         }
-        tc_commit(&bars->s_full[j & 1]);
-        tc_commit(&bars->k_empty[s]);
-        return true;
+        tc_commit(&bars->s_full[t]);
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) ok = issue_qk(j + 1);
-        if (!ok) break;
-        const int s = j % NS;
-        ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort) && mbar_wait(&bars->v_full[s], (j / NS) & 1, abort);
-        if (!ok) break;
+      bool ok = mbar_wait(&bars->q_full, 0, abort) && mbar_wait(&bars->k_full[0], 0, abort);
+      if (ok) {
         tc_fence_after();
-        const uint32_t sP = smem_u32(smem + kOffP + (j & 1) * kPBytes);
-        const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
+        for (int t = 0; t < ntile; ++t) issue_qk(t, 0);
+        tc_commit(&bars->k_empty[0]);
+      }
+      // Per KV tile j and query tile t: PV_t(j) (A = P_t from TMEM), then
+      // QK_t(j+1) into the same TMEM columns.
+      for (int j = 0; ok && j < T; ++j) {
+        const int sv = j % NSV, sk = (j + 1) % NSK;
+        for (int t = 0; ok && t < ntile; ++t) {
+          ok = mbar_wait(&bars->p_full[t], j & 1, abort);
+          if (ok && t == 0) ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sV = smem_u32(smem + kOffV + sv * kVBytes);
 #pragma unroll
-        for (int k = 0; k < BN / 32; ++k)
-          umma_f8f6f4(tmem + kColO, sdesc_sw128(sP + k * 32), sdesc_sw128(sV + k * 32), kIdescPV, (j > 0) || (k > 0));
-        tc_commit(&bars->v_empty[s]);
-        tc_commit(&bars->pv_done);
+          for (int k = 0; k < BN / 32; ++k)
+            umma_f8f6f4_ts(tmem + col_o(t), tmem + col_s(t) + 8 * k, sdesc_sw128(sV + k * 32), kIdescPV,
+                           (j > 0) || (k > 0));
+          if (t == ntile - 1) tc_commit(&bars->v_empty[sv]);
+          if (j + 1 < T) {
+            if (t == 0) ok = mbar_wait(&bars->k_full[sk], ((j + 1) / NSK) & 1, abort);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(t, sk);
+            if (t == ntile - 1) tc_commit(&bars->k_empty[sk]);
+          } else {
+            tc_commit(&bars->o_done[t]);
+          }
+        }
       }
       if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax / correction / epilogue
-    const int r = (warp - 4) * 32 + lane;  // query row in the tile == TMEM lane
-    const int row = q0 + r;
-    const bool valid = row < p.Nq;
-    const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
-    const float sq = valid ? p.q_scales[bh * p.nbq + row / p.q_block] : 0.f;
-    const float *sk = p.k_scales + bh * p.nbk;
-    float m = -INFINITY, l = 0.f;
-    uint8_t *sPbase = smem + kOffP + r * 128;
-    const uint32_t sw = r & 7;
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t S[128];
-      {
-        const uint32_t a = lane_base + ((j & 1) ? kColS1 : kColS0);
-        tmem_ld32(a + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
-        tmem_ld32(a + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
-        tmem_ld32(a + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
-        tmem_ld32(a + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
-        tmem_ld_wait();
-      }
-      // dequantisation multipliers: t = fl(fl(sq * sk) * C) per key block
+    // ------------------------------------------------------------ softmax / rescale / epilogue
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+    if (t < ntile) {
+      const int r = (warp & 3) * 32 + lane;  // row in the tile == TMEM lane
+      const int row = q0 + t * BM + r;
+      const bool valid = row < p.Nq;
+      const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+      const uint32_t colS = lane_base + col_s(t), colO = lane_base + col_o(t);
+      const float sq = valid ? p.q_scales[bh * p.nbq + row / p.q_block] : 0.f;
+      const float *skp = p.k_scales + bh * p.nbk;
+      float m = -INFINITY, l = 0.f;  // l sums 448 * p
+      bool ok = true;
+      // dequantisation multipliers t = fl(fl(sq * sk) * C) of a tile's key blocks
+      auto tile_t = [&](int j, float &lo, float &hi) {
+        if (p.k_block == 128) {
+          lo = hi = __fmul_rn(__fmul_rn(sq, skp[j]), p.C);
+        } else {
+          lo = __fmul_rn(__fmul_rn(sq, skp[2 * j]), p.C);
+          hi = (2 * j + 1 < p.nbk) ? __fmul_rn(__fmul_rn(sq, skp[2 * j + 1]), p.C) : 0.f;
+        }
+      };
       float t_lo, t_hi;
-      if (p.k_block == 128) {
-        t_lo = t_hi = __fmul_rn(__fmul_rn(sq, sk[j]), p.C);
-      } else {
-        t_lo = __fmul_rn(__fmul_rn(sq, sk[2 * j]), p.C);
-        t_hi = (2 * j + 1 < p.nbk) ? __fmul_rn(__fmul_rn(sq, sk[2 * j + 1]), p.C) : 0.f;
-      }
-      const int nvalid = min(BN, p.Nk - j * BN);
-      float s[128];
-      float mt = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        float v = __fmul_rn(__uint_as_float(S[i]), i < 64 ? t_lo : t_hi);
-        if (i >= nvalid) v = -INFINITY;
-        s[i] = v;
-        mt = fmaxf(mt, v);
-      }
-      const float mnew = fmaxf(m, mt);
-      const float alpha = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, mnew));
-      float rowsum = 0.f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float p0 = ex2(__fsub_rn(s[i], mnew));
-        const float p1 = ex2(__fsub_rn(s[i + 1], mnew));
-        const float p2 = ex2(__fsub_rn(s[i + 2], mnew));
-        const float p3 = ex2(__fsub_rn(s[i + 3], mnew));
-        rowsum = __fadd_rn(rowsum, p0);
-        rowsum = __fadd_rn(rowsum, p1);
-        rowsum = __fadd_rn(rowsum, p2);
-        rowsum = __fadd_rn(rowsum, p3);
-        const uint32_t lo = cvt_e4m3x2(__fmul_rn(448.f, p0), __fmul_rn(448.f, p1));
-        const uint32_t hi = cvt_e4m3x2(__fmul_rn(448.f, p2), __fmul_rn(448.f, p3));
-        pk[i >> 2] = lo | (hi << 16);
-      }
-      l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
-      // PV of the previous tile must be complete: it frees this P buffer's
-      // previous user and leaves O stable for the rescale below.
-      if (j >= 1) {
-        ok = mbar_wait(&bars->pv_done, (j - 1) & 1, abort);
+      tile_t(0, t_lo, t_hi);
+      for (int j = 0; j < T; ++j) {
+        ok = mbar_wait(&bars->s_full[t], j & 1, abort);
         if (!ok) break;
         tc_fence_after();
-      }
-      uint8_t *dstP = sPbase + (j & 1) * kPBytes;
+        uint32_t S[128];
+        tmem_ld32(colS + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
+        tmem_ld32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
+        tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
+        tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
+        const int nvalid = min(BN, p.Nk - j * BN);
+        float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
+        if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
+        tmem_ld_wait();
+        float *Sf = reinterpret_cast<float *>(S);
+        const bool masked = nvalid < BN;
+        if (masked) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(dstP + ((c ^ sw) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          for (int i = 0; i < 128; ++i)
+            if (i >= nvalid) Sf[i] = -INFINITY;
+        }
+        // row maximum of the raw scores, four independent chains
+        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
+        float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) {
+          c0 = fmax3(c0, Sf[i], Sf[i + 1]);
+          c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
+          c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
+          c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
+        }
+        const float mlo = fmax3(c0, c1, Sf[31]) , mhi = fmax3(c2, c3, Sf[95]);
+        const float mlo2 = fmax3(mlo, Sf[63], Sf[63]), mhi2 = fmax3(mhi, Sf[127], Sf[127]);
+        const float mt = fmaxf(mlo2 == -INFINITY ? -INFINITY : __fmul_rn(mlo2, t_lo),
+                               mhi2 == -INFINITY ? -INFINITY : __fmul_rn(mhi2, t_hi));
+        const float mnew = fmaxf(m, mt);
+        const float alpha = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, mnew));
+        // x = S * t - (m' - log2 448): 2^x = 448 * p
+        const float nb = __fsub_rn(kLog2_448, mnew);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 128; i += 4) {
+          const float tt = i < 64 ? t_lo : t_hi;
+          float2 x01 = ffma2(make_float2(Sf[i], Sf[i + 1]), make_float2(tt, tt), make_float2(nb, nb));
+          float2 x23 = ffma2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(tt, tt), make_float2(nb, nb));
+          if (masked) {  // keys past Nk: p = 0 (also when t = 0, where -inf * 0 would be NaN)
+            if (i >= nvalid) x01.x = -INFINITY;
+            if (i + 1 >= nvalid) x01.y = -INFINITY;
+            if (i + 2 >= nvalid) x23.x = -INFINITY;
+            if (i + 3 >= nvalid) x23.y = -INFINITY;
+          }
+          const float2 q01 = make_float2(ex2(x01.x), ex2(x01.y));
+          const float2 q23 = make_float2(ex2(x23.x), ex2(x23.y));
+          acc0 = fadd2(acc0, q01);
+          acc1 = fadd2(acc1, q23);
+          pk[i >> 2] = __byte_perm(cvt_e4m3x2(q01.x, q01.y), cvt_e4m3x2(q23.x, q23.y), 0x5410);
+        }
+        const float rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+        l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
+        // P_t over the first 32 columns of S_t (S_t(j) is already in registers;
+        // PV_t(j-1) completed before S_t(j) was committed)
+        tmem_st32(colS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // rescale O_t in TMEM: one load round trip, one store round trip
+          uint32_t o[128];
+          tmem_ld32(colO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_ld32(colO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          tmem_ld32(colO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+          tmem_ld32(colO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+          tmem_ld_wait();
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int i = 0; i < 128; i += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            o[i] = __float_as_uint(v.x);
+            o[i + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(colO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_st32(colO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          tmem_st32(colO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+          tmem_st32(colO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[t]);
+        m = mnew;
+        t_lo = nt_lo;
+        t_hi = nt_hi;
+      }
+      if (ok) ok = mbar_wait(&bars->o_done[t], 0, abort);
+      if (!ok) {
+        report(p.status, SAGE_ERR_TIMEOUT);
+      } else {
+        tc_fence_after();
+        const float *sv = p.v_scales + bh * kD;
+        const int b = bh / p.H, h = bh - b * p.H;
+        __nv_bfloat16 *dst = p.out + b * p.os.b + h * p.os.h + int64_t(row) * p.os.n;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kColO + 32 * c, o);
+          tmem_ld32(colO + 32 * c, o);
           tmem_ld_wait();
+          uint32_t packed[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
-          tmem_st32(lane_base + kColO + 32 * c, o);
-        }
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
-      m = mnew;
-    }
-    if (ok) ok = mbar_wait(&bars->pv_done, (T - 1) & 1, abort);
-    if (!ok) {
-      report(p.status, SAGE_ERR_TIMEOUT);
-    } else {
-      tc_fence_after();
-      const float *sv = p.v_scales + bh * kD;
-      const int b = bh / p.H, h = bh - b * p.H;
-      __nv_bfloat16 *dst = p.out + b * p.os.b + h * p.os.h + int64_t(row) * p.os.n;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-        tmem_ld_wait();
-        uint32_t packed[16];
+          for (int i = 0; i < 32; i += 2) {
+            const float y0 = __fmul_rn(__fdiv_rn(__uint_as_float(o[i]), l), sv[32 * c + i]);
+            const float y1 = __fmul_rn(__fdiv_rn(__uint_as_float(o[i + 1]), l), sv[32 * c + i + 1]);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
+            packed[i >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
+          }
+          if (valid) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float y0 = __fmul_rn(__fdiv_rn(__uint_as_float(o[i]), l), __fdiv_rn(sv[32 * c + i], 448.f));
-          const float y1 =
-              __fmul_rn(__fdiv_rn(__uint_as_float(o[i + 1]), l), __fdiv_rn(sv[32 * c + i + 1], 448.f));
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
-          packed[i >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
-        }
-        if (valid) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * u) =
-                make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * u) =
+                  make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
+          }
         }
       }
     }
@@ -301,6 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -398,7 +451,7 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(ceil_div(a.Nq, BM), BH);
+  dim3 grid(ceil_div(a.Nq, 2 * BM), BH);
   sage_attn_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
