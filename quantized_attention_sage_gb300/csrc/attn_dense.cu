@@ -19,15 +19,13 @@
 //    warps 4-7 and 8-11 are two softmax warpgroups, one per query tile, one
 //    query row per thread (TMEM lane = row).  TMEM: S0, S1, O0, O1, 128
 //    columns each.
-//  * P_t (E4M3) is written by the softmax into TMEM over the first 32 columns
-//    of S_t, whose scores are already in registers; the P.V MMA reads its A
-//    operand from TMEM.
-//  * MMA issue order per KV tile j: PV_t(j) then QK_t(j+1), alternating the
-//    two tiles, so while one warpgroup runs the softmax of its tile the tensor
-//    core works on the other tile (ping-pong).  tcgen05 MMAs issued by one
-//    thread execute in order, so QK_t(j+1) overwrites S_t/P_t only after
-//    PV_t(j) has read P_t, and "S_t(j+1) is ready" implies "PV_t(j) is
-//    complete": the softmax rescales O_t and writes P_t without another wait.
+//  * S_t is free as soon as the softmax has loaded it into registers, so the
+//    MMA warp issues QK_t(j+1) right then (barrier s_free): the next scores
+//    are computed while the softmax of the current tile runs, and the
+//    softmax warps never wait for S after the first tile.  P_t (E4M3) goes to
+//    a 128-byte-swizzled shared tile per query tile, read by PV_t(j).
+//  * The MMA warp is event-driven: it polls the barriers of both query tiles
+//    and issues whichever QK or PV is ready, keeping per-tile order.
 //  * Softmax per element: row max on the raw int32-valued S (the dequant
 //    multiplier is positive, so max(fl(S*t)) = fl(max(S)*t)), one FFMA for
 //    S*t - m' + log2(448), ex2 on MUFU (448*p directly), fp32 row sums of
@@ -41,15 +39,17 @@
 namespace sg {
 namespace dense {
 
-constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
+constexpr int BM = 128, BN = 128, NSK = 3, NSV = 2;
 constexpr int kThreads = 384;
 constexpr uint32_t kQBytes = BM * kD * 2;    // 32 KB fp16 per query tile
 constexpr uint32_t kKBytes = BN * kD * 2;    // 32 KB fp16
 constexpr uint32_t kVBytes = kD * BN;        // 16 KB e4m3
+constexpr uint32_t kPBytes = BM * BN;        // 16 KB e4m3 per query tile
 constexpr uint32_t kOffQ = 0;                // two query tiles
 constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
 constexpr uint32_t kOffV = kOffK + NSK * kKBytes;
-constexpr uint32_t kOffBar = kOffV + NSV * kVBytes;
+constexpr uint32_t kOffP = kOffV + NSV * kVBytes;  // two P tiles
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // barriers + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
@@ -72,7 +72,7 @@ struct Params {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -108,8 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->s_free[t], 4);
       mbar_init(&bars->p_full[t], 4);
-      mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->pv_done[t], 1);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -125,7 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (uniform values); one elected lane issues.
+    const bool leader = elect_one();
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -135,76 +138,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ, &tmQ, &bars->q_full, 0, q0 + t * BM, bh);
         tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0 + t * BM, bh);
       }
-      auto load_k = [&](int j) -> bool {
-        const int s = j % NSK;
-        if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
+    }
+    __syncwarp();
+    auto load_k = [&](int j) -> bool {
+      const int s = j % NSK;
+      if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
+      if (leader) {
         uint8_t *dst = smem + kOffK + s * kKBytes;
         mbar_arrive_expect_tx(&bars->k_full[s], kKBytes);
         tma_load_3d(dst, &tmK, &bars->k_full[s], 0, j * BN, bh);
         tma_load_3d(dst + kKBytes / 2, &tmK, &bars->k_full[s], 64, j * BN, bh);
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int s = j % NSV;
-        if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
+      }
+      __syncwarp();
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int s = j % NSV;
+      if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
+      if (leader) {
         mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
         tma_load_3d(smem + kOffV + s * kVBytes, &tmV, &bars->v_full[s], j * BN, 0, bh);
-        return true;
-      };
-      bool ok = load_k(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
       }
-      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
+      __syncwarp();
+      return true;
+    };
+    bool ok = load_k(0);
+    for (int j = 0; ok && j < T; ++j) {
+      if (j + 1 < T) ok = load_k(j + 1);
+      if (ok) ok = load_v(j);
     }
+    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      auto issue_qk = [&](int t, int s) {
-        const uint32_t sQ = smem_u32(smem + kOffQ + t * kQBytes);
-        const uint32_t sK = smem_u32(smem + kOffK + s * kKBytes);
+    // The whole warp runs the event loop (uniform values); one elected lane
+    // issues the MMAs and commits.
+    const bool leader = elect_one();
+    auto issue_qk = [&](int t, int s) {
+      const uint32_t sQ = smem_u32(smem + kOffQ + t * kQBytes);
+      const uint32_t sK = smem_u32(smem + kOffK + s * kKBytes);
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
           const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
           umma_f16(tmem + col_s(t), sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
         }
         tc_commit(&bars->s_full[t]);
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, abort) && mbar_wait(&bars->k_full[0], 0, abort);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < ntile; ++t) issue_qk(t, 0);
-        tc_commit(&bars->k_empty[0]);
       }
-      // Per KV tile j and query tile t: PV_t(j) (A = P_t from TMEM), then
-      // QK_t(j+1) into the same TMEM columns.
-      for (int j = 0; ok && j < T; ++j) {
-        const int sv = j % NSV, sk = (j + 1) % NSK;
-        for (int t = 0; ok && t < ntile; ++t) {
-          ok = mbar_wait(&bars->p_full[t], j & 1, abort);
-          if (ok && t == 0) ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sV = smem_u32(smem + kOffV + sv * kVBytes);
+      __syncwarp();
+    };
+    bool ok = mbar_wait(&bars->q_full, 0, abort) && mbar_wait(&bars->k_full[0], 0, abort);
+    if (ok) {
+      tc_fence_after();
+      for (int t = 0; t < ntile; ++t) issue_qk(t, 0);
+      if (leader) tc_commit(&bars->k_empty[0]);
+      __syncwarp();
+    }
+    // Event loop.  QK_t(j) needs K_j and the softmax's load of S_t(j-1)
+    // (s_free); PV_t(j) needs P_t(j) (p_full) and V_j.  A K or V stage is
+    // released after its last user among the query tiles is issued: with two
+    // tiles, the second user of a stage is the one whose partner already
+    // passed it.
+    int qk0 = 1, qk1 = ntile == 2 ? 1 : T, pv0 = 0, pv1 = ntile == 2 ? 0 : T;
+    uint64_t idle_since = 0;
+    while (ok && (pv0 < T || pv1 < T)) {
+      bool progress = false;
 #pragma unroll
-          for (int k = 0; k < BN / 32; ++k)
-            umma_f8f6f4_ts(tmem + col_o(t), tmem + col_s(t) + 8 * k, sdesc_sw128(sV + k * 32), kIdescPV,
-                           (j > 0) || (k > 0));
-          if (t == ntile - 1) tc_commit(&bars->v_empty[sv]);
-          if (j + 1 < T) {
-            if (t == 0) ok = mbar_wait(&bars->k_full[sk], ((j + 1) / NSK) & 1, abort);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(t, sk);
-            if (t == ntile - 1) tc_commit(&bars->k_empty[sk]);
-          } else {
-            tc_commit(&bars->o_done[t]);
+      for (int t = 0; t < 2; ++t) {
+        const int jq = t ? qk1 : qk0;
+        const int jq_other = t ? qk0 : qk1;
+        if (jq < T && mbar_test(&bars->s_free[t], (jq - 1) & 1) &&
+            mbar_test(&bars->k_full[jq % NSK], (jq / NSK) & 1)) {
+          tc_fence_after();
+          issue_qk(t, jq % NSK);
+          if (ntile == 1 || jq_other > jq) {  // last user of K stage jq
+            if (leader) tc_commit(&bars->k_empty[jq % NSK]);
+            __syncwarp();
           }
+          if (t) qk1 = jq + 1; else qk0 = jq + 1;
+          progress = true;
+        }
+        const int jp = t ? pv1 : pv0;
+        const int jp_other = t ? pv0 : pv1;
+        if (jp < T && mbar_test(&bars->p_full[t], jp & 1) && mbar_test(&bars->v_full[jp % NSV], (jp / NSV) & 1)) {
+          tc_fence_after();
+          const uint32_t sP = smem_u32(smem + kOffP + t * kPBytes);
+          const uint32_t sV = smem_u32(smem + kOffV + (jp % NSV) * kVBytes);
+          if (leader) {
+#pragma unroll
+            for (int k = 0; k < BN / 32; ++k)
+              umma_f8f6f4(tmem + col_o(t), sdesc_sw128(sP + k * 32), sdesc_sw128(sV + k * 32), kIdescPV,
+                          (jp > 0) || (k > 0));
+            tc_commit(&bars->pv_done[t]);
+            if (ntile == 1 || jp_other > jp) tc_commit(&bars->v_empty[jp % NSV]);
+          }
+          __syncwarp();
+          if (t) pv1 = jp + 1; else pv0 = jp + 1;
+          progress = true;
         }
       }
-      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
+      if (progress) {
+        idle_since = 0;
+      } else {
+        __nanosleep(32);  // leave issue slots to the softmax warps of this sub-partition
+        const uint64_t now = globaltimer();
+        if (idle_since == 0) idle_since = now;
+        else if (now - idle_since > kWaitLimitNs || *abort) ok = false;
+      }
     }
+    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / rescale / epilogue
     const int t = (warp - 4) >> 2;  // query tile of this warpgroup
@@ -214,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < p.Nq;
       const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
       const uint32_t colS = lane_base + col_s(t), colO = lane_base + col_o(t);
+      uint8_t *sP = smem + kOffP + t * kPBytes + r * 128;
+      const uint32_t sw = r & 7;
       const float sq = valid ? p.q_scales[bh * p.nbq + row / p.q_block] : 0.f;
       const float *skp = p.k_scales + bh * p.nbk;
       float m = -INFINITY, l = 0.f;  // l sums 448 * p
@@ -242,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait();
+        // S_t(j) is in registers: the MMA warp may compute S_t(j+1) now
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[t]);
         float *Sf = reinterpret_cast<float *>(S);
         const bool masked = nvalid < BN;
         if (masked) {
@@ -288,9 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
         l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
-        // P_t over the first 32 columns of S_t (S_t(j) is already in registers;
-        // PV_t(j-1) completed before S_t(j) was committed)
-        tmem_st32(colS, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        // PV_t(j-1) must be complete: it read P_t and accumulated into O_t
+        if (j >= 1) {
+          ok = mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4 *>(sP + ((c ^ sw) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
         if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // rescale O_t in TMEM: one load round trip, one store round trip
           uint32_t o[128];
@@ -310,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(colO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
           tmem_st32(colO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
           tmem_st32(colO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+          tmem_st_wait();
         }
-        tmem_st_wait();
+        fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[t]);
@@ -319,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         t_lo = nt_lo;
         t_hi = nt_hi;
       }
-      if (ok) ok = mbar_wait(&bars->o_done[t], 0, abort);
+      if (ok) ok = mbar_wait(&bars->pv_done[t], (T - 1) & 1, abort);
       if (!ok) {
         report(p.status, SAGE_ERR_TIMEOUT);
       } else {
