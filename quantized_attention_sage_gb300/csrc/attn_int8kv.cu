@@ -13,10 +13,14 @@
 //    int8 K codes), fp32 in TMEM.
 //  * softmax per row in fp32: s = S * fl(ks * sm_scale * log2 e), causal mask
 //    by absolute position, p = 2^(s - m).
-//  * P.V: the weight w = p * vs (scaled by a power of two so that w < 2) is
+//  * P.V: the weight w = p * vs (scaled by a power of two so that w < 1) is
 //    split into fp16 hi + lo parts and multiplied with exact fp16 images of the
 //    V codes by one K = 256 kind::f16 MMA chain ([hi | lo] . [V ; V]), so the
-//    fp16 rounding of w does not reach the output.
+//    fp16 rounding of w does not reach the output.  hi and lo are written
+//    with tcgen05.st over the consumed S buffer and read by the MMA from TMEM.
+//  * S is double-buffered in TMEM and QK(j+2) is issued right behind PV(j),
+//    so the next scores are ready when the softmax finishes a tile; the MMA
+//    and TMA warps run converged with one elected lane issuing.
 //  * The key range of each query tile is split into `nsplit` contiguous pieces
 //    (split-KV) so the grid fills the SMs; a combine kernel merges the (m, l,
 //    O) partials of one row in split order.
@@ -29,22 +33,22 @@
 namespace sg {
 namespace kv {
 
-constexpr int BM = 128, BN = 128;
+constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
 constexpr int kThreads = 256;
 constexpr uint32_t kQBytes = BM * kD * 2;
-constexpr uint32_t kKTile = BN * kD * 2;
+constexpr uint32_t kKTile = BN * kD * 2;                // bf16 K image
 constexpr uint32_t kVBytes = kD * BN * 2;               // fp16 V^T image
-constexpr uint32_t kPBytes = BM * BN * 2;               // one fp16 P tile
-constexpr uint32_t kPBuf = 2 * kPBytes;                 // hi + lo
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + kKTile;
-constexpr uint32_t kOffP = kOffV + kVBytes;             // two buffers of (hi, lo)
-constexpr uint32_t kOffBar = kOffP + 2 * kPBuf;
+constexpr uint32_t kOffV = kOffK + NSK * kKTile;
+constexpr uint32_t kOffBar = kOffV + NSV * kVBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+// TMEM: S double buffer at columns 0 and 128, O at 256.  P_j (fp16 hi in the
+// first 64 columns, lo in the next 64) overwrites the consumed S_j buffer.
+__host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
+constexpr uint32_t kColO = 256;
 
 constexpr uint32_t kIdescQK = make_idesc(kFmtF32, kFmtBF16, kFmtBF16, BM, BN);
 constexpr uint32_t kIdescPV = make_idesc(kFmtF32, kFmtF16, kFmtF16, BM, kD);
@@ -60,14 +64,12 @@ struct Params {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full, k_empty;
-  uint64_t v_full, v_empty;
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
+  uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
+  uint64_t s_full[2], p_full, pv_done;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 __device__ __forceinline__ void report(int32_t *status, int code) {
   if (status) atomicCAS(status, 0, code);
@@ -97,15 +99,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
-    mbar_init(&bars->k_full, 1);
-    mbar_init(&bars->k_empty, 1);
-    mbar_init(&bars->v_full, 1);
-    mbar_init(&bars->v_empty, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 4);
-      mbar_init(&bars->pv_done[b], 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
     }
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    mbar_init(&bars->s_full[0], 1);
+    mbar_init(&bars->s_full[1], 1);
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->pv_done, 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -125,77 +130,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       p.part_ml[int64_t(unit) * BM + r] = make_float2(-INFINITY, 0.f);
     }
   } else if (warp == 0) {
-    if (lane == 0) {
+    // ------------------------------------------------------------ TMA producer (converged warp)
+    const bool leader = elect_one();
+    if (leader) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(&bars->q_full, uint32_t(p.QT * p.G) * 256u);
       tma_load_3d(smem + kOffQ, &tmQ, &bars->q_full, 0, g * p.G, i0);
       tma_load_3d(smem + kOffQ + kQBytes / 2, &tmQ, &bars->q_full, 64, g * p.G, i0);
-      auto load_k = [&](int j) -> bool {
-        if (j >= 1 && !mbar_wait(&bars->k_empty, (j - 1) & 1, abort)) return false;
-        const int key0 = (tb + j) * BN;
-        mbar_arrive_expect_tx(&bars->k_full, kKTile);
-        tma_load_3d(smem + kOffK, &tmK, &bars->k_full, 0, key0, g);
-        tma_load_3d(smem + kOffK + kKTile / 2, &tmK, &bars->k_full, 64, key0, g);
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        if (j >= 1 && !mbar_wait(&bars->v_empty, (j - 1) & 1, abort)) return false;
-        mbar_arrive_expect_tx(&bars->v_full, kVBytes);
-        const int key0 = (tb + j) * BN;
-        tma_load_3d(smem + kOffV, &tmV, &bars->v_full, key0, 0, g);
-        tma_load_3d(smem + kOffV + kVBytes / 2, &tmV, &bars->v_full, key0 + 64, 0, g);
-        return true;
-      };
-      bool ok = load_k(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
-      }
-      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
     }
+    __syncwarp();
+    auto load_k = [&](int j) -> bool {
+      const int s = j % NSK;
+      if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
+      if (leader) {
+        const int key0 = (tb + j) * BN;
+        uint8_t *dst = smem + kOffK + s * kKTile;
+        mbar_arrive_expect_tx(&bars->k_full[s], kKTile);
+        tma_load_3d(dst, &tmK, &bars->k_full[s], 0, key0, g);
+        tma_load_3d(dst + kKTile / 2, &tmK, &bars->k_full[s], 64, key0, g);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      const int s = j % NSV;
+      if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
+      if (leader) {
+        const int key0 = (tb + j) * BN;
+        uint8_t *dst = smem + kOffV + s * kVBytes;
+        mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
+        tma_load_3d(dst, &tmV, &bars->v_full[s], key0, 0, g);
+        tma_load_3d(dst + kVBytes / 2, &tmV, &bars->v_full[s], key0 + 64, 0, g);
+      }
+      __syncwarp();
+      return true;
+    };
+    // order of first use: K0, K1, V0, K2, V1, K3, ...
+    bool ok = load_k(0) && (T < 2 || load_k(1));
+    for (int j = 0; ok && j < T; ++j) {
+      ok = load_v(j);
+      if (ok && j + 2 < T) ok = load_k(j + 2);
+    }
+    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t sQ = smem_u32(smem + kOffQ);
-      auto issue_qk = [&](int j) -> bool {
-        if (!mbar_wait(&bars->k_full, j & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t sK = smem_u32(smem + kOffK);
-        const uint32_t dS = tmem + ((j & 1) ? kColS1 : kColS0);
+    // ------------------------------------------------------------ MMA issuer (converged warp)
+    // Order: QK(0), QK(1), then per tile j: PV(j) (A = P_j from TMEM), QK(j+2)
+    // into the same TMEM buffer (MMAs of one thread execute in order, so
+    // QK(j+2) overwrites P_j only after PV(j) has read it).
+    const bool leader = elect_one();
+    const uint32_t sQ = smem_u32(smem + kOffQ);
+    auto issue_qk = [&](int j) -> bool {
+      const int s = j % NSK;
+      if (!mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort)) return false;
+      tc_fence_after();
+      const uint32_t sK = smem_u32(smem + kOffK + s * kKTile);
+      if (leader) {
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
           const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
-          umma_f16(dS, sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
+          umma_f16(tmem + col_s(j & 1), sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
         }
         tc_commit(&bars->s_full[j & 1]);
-        tc_commit(&bars->k_empty);
-        return true;
-      };
-      bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) ok = issue_qk(j + 1);
-        if (!ok) break;
-        ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort) && mbar_wait(&bars->v_full, j & 1, abort);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sP = smem_u32(smem + kOffP + (j & 1) * kPBuf);
-        const uint32_t sV = smem_u32(smem + kOffV);
+        tc_commit(&bars->k_empty[s]);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0) && (T < 2 || issue_qk(1));
+    for (int j = 0; ok && j < T; ++j) {
+      const int s = j % NSV;
+      ok = mbar_wait(&bars->p_full, j & 1, abort) && mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
+      if (leader) {
+        // O += [P_hi | P_lo] . [V ; V]: 8 K-steps over P_hi then 8 over P_lo
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hl = 0; hl < 2; ++hl) {
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k) {
-            const uint32_t off = (k >> 2) * (kPBytes / 2) + (k & 3) * 32;
-            umma_f16(tmem + kColO, sdesc_sw128(sP + half * kPBytes + off), sdesc_sw128(sV + off), kIdescPV,
-                     (j > 0) || (half > 0) || (k > 0));
+            const uint32_t off = (k >> 2) * (kVBytes / 2) + (k & 3) * 32;
+            umma_f16_ts(tmem + kColO, tmem + col_s(j & 1) + 64 * hl + 8 * k, sdesc_sw128(sV + off), kIdescPV,
+                        (j > 0) || (hl > 0) || (k > 0));
           }
         }
-        tc_commit(&bars->v_empty);
-        tc_commit(&bars->pv_done[j & 1]);
+        tc_commit(&bars->pv_done);
+        tc_commit(&bars->v_empty[s]);
       }
-      if (!ok) report(p.status, SAGE_ERR_TIMEOUT);
+      __syncwarp();
+      if (j + 2 < T) ok = issue_qk(j + 2);
     }
+    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / rescale / partials
     const int r = (warp - 4) * 32 + lane;
     const int il = r / p.G;
     const int qi = i0 + il;
@@ -209,113 +238,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float *kt_row = p.kt + int64_t(g) * p.Npad;
     const float *vs_row = p.vs + int64_t(g) * p.Npad;
     float m = -INFINITY, l = 0.f;
-    const uint32_t sw = r & 7;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
       ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sa = lane_base + ((j & 1) ? kColS1 : kColS0);
+      const uint32_t sa = lane_base + col_s(j & 1);
+      uint32_t S[128];
+      tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
+      tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
+      tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
+      tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
       const int key0 = (tb + j) * BN;
       const float *kt = kt_row + key0;
       const float *vsc = vs_row + key0;
       const int nvis = min(BN, pos - key0 + 1);  // visible keys of this tile (<= 0: none)
-      // pass 1: row maximum of s = S * kt over the visible keys
+      tmem_ld_wait();
+      float *Sf = reinterpret_cast<float *>(S);
+      // s = S * kt (base-2 logits), masked past the query's position
       float mt = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t S[32];
-        tmem_ld32(sa + 32 * c, S);
-        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + 32 * c + i));
-          const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float v = __fmul_rn(__uint_as_float(S[i + u]), kk[u]);
-            if (32 * c + i + u < nvis) mt = fmaxf(mt, v);
-          }
-        }
+      for (int i = 0; i < 128; i += 4) {
+        const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + i));
+        Sf[i] = __fmul_rn(Sf[i], k4.x);
+        Sf[i + 1] = __fmul_rn(Sf[i + 1], k4.y);
+        Sf[i + 2] = __fmul_rn(Sf[i + 2], k4.z);
+        Sf[i + 3] = __fmul_rn(Sf[i + 3], k4.w);
       }
+      if (nvis < BN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= nvis) Sf[i] = -INFINITY;
+      }
+#pragma unroll
+      for (int i = 0; i < 128; i += 2) mt = fmax3(mt, Sf[i], Sf[i + 1]);
       const float mnew = fmaxf(m, mt);
       const float alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
       const float msub = (mnew == -INFINITY) ? 0.f : mnew;
-      // P buffer j&1 was last read by PV_{j-2}
-      if (j >= 2) {
-        ok = mbar_wait(&bars->pv_done[j & 1], ((j >> 1) + 1) & 1, abort);
-        if (!ok) break;
-      }
-      // pass 2: p = 2^(s - m'), row sum, w = p * vs * 2^-E split into fp16
-      // hi + lo and written to the swizzled P tiles (hi at +0, lo at +kPBytes;
-      // each tile is two 64-key column blocks of 128-byte rows)
+      // p = 2^(s - m'), row sum, w = p * vs * 2^-E split into fp16 hi + lo,
+      // written over this S buffer: hi at columns 0-63, lo at 64-127
       float rowsum = 0.f;
-      uint8_t *dstP = smem + kOffP + (j & 1) * kPBuf + r * 128;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t S[32];
-        tmem_ld32(sa + 32 * c, S);
-        tmem_ld_wait();
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-          uint32_t hi[4], lo[4];
+        for (int i = 0; i < 32; i += 4) {
+          const float4 v4 = __ldg(reinterpret_cast<const float4 *>(vsc + 32 * c + i));
+          const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
+          float w[4];
 #pragma unroll
-          for (int u4 = 0; u4 < 8; u4 += 4) {
-            const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + 32 * c + i + u4));
-            const float4 v4 = __ldg(reinterpret_cast<const float4 *>(vsc + 32 * c + i + u4));
-            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-            const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float v = __fmul_rn(__uint_as_float(S[i + u4 + u]), kk[u]);
-              if (32 * c + i + u4 + u >= nvis) v = -INFINITY;
-              const float pe = ex2(__fsub_rn(v, msub));
-              rowsum = __fadd_rn(rowsum, pe);
-              w[u] = __fmul_rn(pe, __fmul_rn(vv[u], wscale));
-            }
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              const __half2 h = __floats2half2_rn(w[u], w[u + 1]);
-              const float2 hf = __half22float2(h);
-              const __half2 lw = __floats2half2_rn(__fsub_rn(w[u], hf.x), __fsub_rn(w[u + 1], hf.y));
-              hi[(u4 + u) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
-              lo[(u4 + u) >> 1] = *reinterpret_cast<const uint32_t *>(&lw);
-            }
+          for (int u = 0; u < 4; ++u) {
+            const float pe = ex2(__fsub_rn(Sf[32 * c + i + u], msub));
+            rowsum = __fadd_rn(rowsum, pe);
+            w[u] = __fmul_rn(pe, __fmul_rn(vv[u], wscale));
           }
-          const int key = 32 * c + i;          // first of the 8 keys of this 16-byte chunk
-          const int cb = key >> 6, ch = (key & 63) >> 3;
-          uint8_t *d = dstP + cb * (kPBytes / 2) + ((ch ^ sw) << 4);
-          *reinterpret_cast<uint4 *>(d) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4 *>(d + kPBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            const __half2 h = __floats2half2_rn(w[u], w[u + 1]);
+            const float2 hf = __half22float2(h);
+            const __half2 lw = __floats2half2_rn(__fsub_rn(w[u], hf.x), __fsub_rn(w[u + 1], hf.y));
+            hi[(i + u) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
+            lo[(i + u) >> 1] = *reinterpret_cast<const uint32_t *>(&lw);
+          }
         }
+        tmem_st16(sa + 16 * c, hi);
+        tmem_st16(sa + 64 + 16 * c, lo);
       }
       l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
-      // O is stable once PV_{j-1} is complete; rescale it when the max grew
-      if (j >= 1) {
-        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+      // O is stable once PV(j-1) is complete; rescale it when the max grew
+      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        ok = mbar_wait(&bars->pv_done, (j - 1) & 1, abort);
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + kColO + 32 * c, o);
-            tmem_ld_wait();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kColO + 32 * c, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
-            tmem_st32(lane_base + kColO + 32 * c, o);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
+          tmem_st32(lane_base + kColO + 32 * c, o);
         }
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full);
       m = mnew;
     }
-    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    if (ok) ok = mbar_wait(&bars->pv_done, (T - 1) & 1, abort);
     if (!ok) {
       report(p.status, SAGE_ERR_TIMEOUT);
     } else {
