@@ -173,6 +173,22 @@ sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const in
                           size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_attn_fwd_scores_dump - sage_attn_fwd that also writes, for checking,
+ * every exact integer score S = q_codes . k_codes^T the tensor cores produced
+ * for the attention (the Q.K^T of the defining passage above), as int32 into
+ * s_dump [B*H][Nq_pad][Nk_pad] with Nq_pad = ceil(Nq/256)*256 and
+ * Nk_pad = ceil(Nk/128)*128 (entries past Nq or Nk are scores against zero
+ * rows).  Diagnostic only: the dump costs a full write of S and is meant for
+ * small problems.  s_dump must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+sage_status sage_attn_fwd_scores_dump(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                                      const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                                      int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
+                                      float sm_scale, void *out_bf16, sage_strides os, void *workspace,
+                                      size_t workspace_bytes, int32_t *status_dev, int32_t *s_dump,
+                                      void *stream);
+
+/* ------------------------------------------------------------------------
  * int8kv_prompt_attn - causal prompt attention of bf16 queries over an int8
  * KV cache with per-token fp16 scales, grouped-query heads.
  *

@@ -78,6 +78,9 @@ def lib():
     L.sage_attn_fwd.restype = i32
     L.sage_attn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                 vp, Strides, vp, sz, vp, vp]
+    L.sage_attn_fwd_scores_dump.restype = i32
+    L.sage_attn_fwd_scores_dump.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                            vp, Strides, vp, sz, vp, vp, vp]
     L.int8kv_prompt_attn_workspace.restype = sz
     L.int8kv_prompt_attn_workspace.argtypes = [i32, i32, i32, i32]
     L.int8kv_prompt_attn.restype = i32
@@ -190,6 +193,29 @@ def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_s
                            float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
                            _stream(stream)), "sage_attn_fwd")
     return out
+
+
+def sage_attn_fwd_scores_dump(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
+                              stream=None):
+    """sage_attn_fwd plus the exact int32 scores Q.K^T the tensor cores produced.
+
+    Returns (out bf16 [B,H,Nq,128], scores int32 [B,H,Nq_pad,Nk_pad]).  For checking small problems."""
+    torch = _torch()
+    qc, kc = qk["q_codes"], qk["k_codes"]
+    B, H, Nq, _ = qc.shape
+    Nk = kc.shape[2]
+    dev = qc.device
+    out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=dev)
+    nq_pad = (Nq + 255) // 256 * 256
+    scores = torch.zeros((B, H, nq_pad, nk_pad(Nk)), dtype=torch.int32, device=dev)
+    L = lib()
+    nbytes = L.sage_attn_fwd_workspace(B, H, Nq, Nk)
+    ws = _workspace(nbytes, dev)
+    _check(L.sage_attn_fwd_scores_dump(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
+                                       _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block,
+                                       k_block, float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes,
+                                       None, _ptr(scores), _stream(stream)), "sage_attn_fwd_scores_dump")
+    return out, scores
 
 
 def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,

@@ -146,11 +146,11 @@ size_t sage_attn_fwd_workspace(int B, int H, int Nq, int Nk) {
   return dense_workspace_bytes(B, H, Nq, Nk);
 }
 
-sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
-                          const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
-                          int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
-                          sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
-                          void *stream) {
+static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                                 const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
+                                 int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
+                                 sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                                 int32_t *s_dump, void *stream) {
   if (d != kD) return SAGE_ERR_UNSUPPORTED;
   if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
   if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
@@ -179,8 +179,30 @@ sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const in
   a.q_img = ws;
   a.k_img = ws + size_t(B) * H * Nq * kD * 2;
   a.status = status_dev;
+  a.s_dump = s_dump;
   return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
 }
+
+sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                          const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
+                          int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
+                          sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                          void *stream) {
+  return attn_fwd_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, B, H, Nq, Nk, d, q_block, k_block,
+                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, nullptr, stream);
+}
+
+sage_status sage_attn_fwd_scores_dump(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                                      const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B,
+                                      int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale,
+                                      void *out_bf16, sage_strides os, void *workspace, size_t workspace_bytes,
+                                      int32_t *status_dev, int32_t *s_dump, void *stream) {
+  if (s_dump == nullptr || (reinterpret_cast<uintptr_t>(s_dump) & 15u)) return SAGE_ERR_INVALID_ARG;
+  return attn_fwd_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, B, H, Nq, Nk, d, q_block, k_block,
+                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, s_dump, stream);
+}
+
+
 
 size_t int8kv_prompt_attn_workspace(int Nq, int Hq, int Hkv, int Nk) {
   if (Nq < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return 0;

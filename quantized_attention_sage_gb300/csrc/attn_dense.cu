@@ -67,6 +67,8 @@ struct Params {
   __nv_bfloat16 *out;
   sage_strides os;
   int32_t *status;
+  int32_t *s_dump;  // diagnostic: exact scores [B*H][Nq_pad][Nk_pad], or null
+  int nq_pad, nk_pad;
 };
 
 struct Bars {
@@ -285,6 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait();
+        if (p.s_dump != nullptr) {  // diagnostic copy of the exact integer scores
+          int32_t *d = p.s_dump + (int64_t(bh) * p.nq_pad + (q0 + t * BM + r)) * p.nk_pad + j * BN;
+#pragma unroll
+          for (int i = 0; i < 128; i += 4)
+            *reinterpret_cast<int4 *>(d + i) =
+                make_int4(__float2int_rn(__uint_as_float(S[i])), __float2int_rn(__uint_as_float(S[i + 1])),
+                          __float2int_rn(__uint_as_float(S[i + 2])), __float2int_rn(__uint_as_float(S[i + 3])));
+        }
         // S_t(j) is in registers: the MMA warp may compute S_t(j+1) now
         tc_fence_before();
         __syncwarp();
@@ -499,6 +509,9 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.os = a.os;
   p.status = a.status;
+  p.s_dump = a.s_dump;
+  p.nq_pad = ceil_div(a.Nq, 2 * BM) * 2 * BM;
+  p.nk_pad = npad;
 
   static bool attr_set = false;
   if (!attr_set) {

@@ -44,6 +44,7 @@ struct DenseArgs {
   sage_strides os;
   void *q_img, *k_img;  // workspace: fp16 images of the codes
   int32_t *status;
+  int32_t *s_dump = nullptr;  // diagnostic score dump or null
 };
 size_t dense_workspace_bytes(int B, int H, int Nq, int Nk);
 cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st);

@@ -88,7 +88,7 @@ struct QKQuantArgs {
 };
 
 template <int BLK>
-__global__ void __launch_bounds__(256) quant_qk_kernel(const QKQuantArgs a) {
+__global__ void __launch_bounds__(256, 4) quant_qk_kernel(const QKQuantArgs a) {
   constexpr int CH = BLK * 16 / 256;  // 16-byte chunks per thread
   __shared__ float red[8];
   const bool isk = int(blockIdx.x) >= a.nbq;
@@ -100,31 +100,37 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const QKQuantArgs a) {
   const __nv_bfloat16 *src = (isk ? a.k : a.q) + b * s.b + h * s.h;
   const int t0 = blk * BLK;
   const int nt = min(BLK, N - t0);
-
-  float x[CH][8];
+  // every thread owns one 8-channel column group: col = (tid & 15) * 8
+  const int col = (threadIdx.x & 15) * 8;
+  float mu[8];
+  if (isk) {
+    const float4 m0 = *reinterpret_cast<const float4 *>(a.mean + bh * kD + col);
+    const float4 m1 = *reinterpret_cast<const float4 *>(a.mean + bh * kD + col + 4);
+    mu[0] = m0.x, mu[1] = m0.y, mu[2] = m0.z, mu[3] = m0.w, mu[4] = m1.x, mu[5] = m1.y, mu[6] = m1.z, mu[7] = m1.w;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mu[j] = 0.f;
+  }
+  // raw bf16 chunks stay packed in registers; both passes convert on the fly
+  uint4 raw[CH];
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int row = (threadIdx.x >> 4) + 16 * i;
+    raw[i] = row < nt ? *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * s.n + col)
+                      : make_uint4(0u, 0u, 0u, 0u);
+  }
+  auto value = [&](const uint4 &w, int j) -> float {
+    const uint32_t word = j < 2 ? w.x : j < 4 ? w.y : j < 6 ? w.z : w.w;
+    const float f = __uint_as_float((j & 1) ? (word & 0xFFFF0000u) : (word << 16));
+    return isk ? __fsub_rn(f, mu[j]) : f;
+  };
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
-    const int e = threadIdx.x + 256 * i;
-    const int row = e >> 4, col = (e & 15) * 8;
+    const int row = (threadIdx.x >> 4) + 16 * i;
     if (row < nt) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * s.n + col);
-      const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(v2[j]);
-        x[i][2 * j] = f.x;
-        x[i][2 * j + 1] = f.y;
-      }
-      if (isk) {
-        const float4 m0 = *reinterpret_cast<const float4 *>(a.mean + bh * kD + col);
-        const float4 m1 = *reinterpret_cast<const float4 *>(a.mean + bh * kD + col + 4);
-        const float m[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x[i][j] = __fsub_rn(x[i][j], m[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[i][j]));
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(value(raw[i], j)));
     }
   }
 #pragma unroll
@@ -143,13 +149,12 @@ __global__ void __launch_bounds__(256) quant_qk_kernel(const QKQuantArgs a) {
   int8_t *dst = (isk ? a.k_codes : a.q_codes) + (int64_t(bh) * N + t0) * kD;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
-    const int e = threadIdx.x + 256 * i;
-    const int row = e >> 4, col = (e & 15) * 8;
+    const int row = (threadIdx.x >> 4) + 16 * i;
     if (row < nt) {
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        int c = __float2int_rn(__fmul_rn(x[i][j], inv));
+        int c = __float2int_rn(__fmul_rn(value(raw[i], j), inv));
         c = max(-127, min(127, c));
         w[j >> 2] |= (uint32_t(c) & 0xFFu) << (8 * (j & 3));
       }

@@ -119,3 +119,23 @@ def test_dense_full_size_videodit_sampled(cuda_lib):
         _, rel64 = errors(got, f64)
         print(f"videodit h{h}: vs oracle max-abs {max_abs:.2e} rel-L2 {rel:.2e}; vs fp64 attention rel-L2 {rel64:.3e}")
         assert rel64 < 0.1
+
+
+@pytest.mark.parametrize("name", ["tiny_b1h2n256", "sweep_b1h4n1", "sweep_b1h4n129", "sweep_b1h4n257"])
+def test_dense_int32_scores_are_exact(cuda_lib, name):
+    """The scores the tensor cores produce (kind::f16 over fp16 images of the
+    INT8 codes) equal the exact integer dot products of the oracle's codes."""
+    w = synth.dense_workload(name)
+    x = synth.dense_inputs(w)
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), w.block, w.block)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    out, scores = cuda_lib.sage_attn_fwd_scores_dump(qk, vq, w.block, w.block)
+    out_ref = cuda_lib.sage_attn_fwd(qk, vq, w.block, w.block)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out_ref.view(torch.int16))
+    for h in range(w.H):
+        ref = oracle.sage_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.block, w.block, rows=[0])
+        exact = ref["qc"].astype(np.int64) @ ref["kc"].astype(np.int64).T
+        got = scores[0, h, :w.Nq, :w.Nk].cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, exact), f"{name} h{h}"
+        assert np.abs(exact).max() <= 128 * 127 * 127
