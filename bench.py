@@ -194,6 +194,28 @@ def run_reference(args, rank):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank timing: every rank runs the whole workload on its own GPU (the
+# (b, h) problems are independent, no collective on the data path); the job's
+# time is the slowest rank's and the value counts the work of all ranks
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(ms: float, dist=None, device=None) -> float:
+    """The maximum of a per-rank time over all ranks (the value itself without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: int, world: int, ms: float) -> float:
+    """Aggregate throughput: the work of all ranks over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
 
@@ -274,11 +296,7 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     assert status.item() == 0, "device status set during the timed steps"
     ms_step = ms_total / args.steps
     comp = {
@@ -286,7 +304,7 @@ def run_ours(args, rank, world):
         "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
         "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
     }
-    value = world * w.flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(w.flops, world, ms_step)
 
     # ---- end to end through the public API with pinned host buffers
     hout = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
@@ -311,12 +329,8 @@ def run_ours(args, rank, world):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e = {"value": world * w.flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_e2e,
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e = {"value": whole_job_tflops(w.flops, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
 
     # ---- int8 KV-cache prompt attention

@@ -175,14 +175,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the event loop (uniform values); one elected lane
     // issues the MMAs and commits.
     const bool leader = elect_one();
+    // Shared-memory descriptors are built once; a K-step only adds a constant:
+    // +32 bytes (2 in the address field) inside a 128-byte swizzle row, +16 KB
+    // (1024) to the second 64-column block of an fp16 tile.
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + kOffQ));
+    const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kOffK));
+    const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kOffV));
+    const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kOffP));
+    constexpr uint64_t kQStep = kQBytes >> 4, kKStep = kKBytes >> 4, kVStep = kVBytes >> 4, kPStep = kPBytes >> 4;
     auto issue_qk = [&](int t, int s) {
-      const uint32_t sQ = smem_u32(smem + kOffQ + t * kQBytes);
-      const uint32_t sK = smem_u32(smem + kOffK + s * kKBytes);
+      const uint64_t dq = dQ0 + uint64_t(t) * kQStep, dk = dK0 + uint64_t(s) * kKStep;
+      const uint32_t dS = tmem + col_s(t);
       if (leader) {
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
-          umma_f16(tmem + col_s(t), sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
+          const uint64_t off = uint64_t((k >> 2) * (kQBytes / 2 / 16) + (k & 3) * 2);
+          umma_f16(dS, dq + off, dk + off, kIdescQK, k > 0);
         }
         tc_commit(&bars->s_full[t]);
       }
@@ -223,13 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jp_other = t ? pv0 : pv1;
         if (jp < T && mbar_test(&bars->p_full[t], jp & 1) && mbar_test(&bars->v_full[jp % NSV], (jp / NSV) & 1)) {
           tc_fence_after();
-          const uint32_t sP = smem_u32(smem + kOffP + t * kPBytes);
-          const uint32_t sV = smem_u32(smem + kOffV + (jp % NSV) * kVBytes);
+          const uint64_t dp = dP0 + uint64_t(t) * kPStep, dv = dV0 + uint64_t(jp % NSV) * kVStep;
           if (leader) {
 #pragma unroll
             for (int k = 0; k < BN / 32; ++k)
-              umma_f8f6f4(tmem + col_o(t), sdesc_sw128(sP + k * 32), sdesc_sw128(sV + k * 32), kIdescPV,
-                          (jp > 0) || (k > 0));
+              umma_f8f6f4(tmem + col_o(t), dp + uint64_t(2 * k), dv + uint64_t(2 * k), kIdescPV, (jp > 0) || (k > 0));
             tc_commit(&bars->pv_done[t]);
             if (ntile == 1 || jp_other > jp) tc_commit(&bars->v_empty[jp % NSV]);
           }
