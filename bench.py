@@ -45,10 +45,12 @@ METRIC = "quantized attention fwd effective TFLOPS (4*Nq*Nk*d*H), video-DiT 37,8
 UNIT = "TFLOP/s"
 WORKLOAD = "videodit_b1h24n37810"
 
-# dram bytes (read + write) per launch of the attention call, from one ncu
-# capture of the kernel source with this sha256 prefix; None when the source
-# has changed since.
-TRAFFIC = {"sha256_prefix": None, "bytes": None}
+# dram bytes (read + write) per sage_attn_fwd call (two code->fp16 image
+# passes + the attention kernel), from one ncu capture of the 24-head,
+# 8192-token case scaled by 37810/8192 (every head's inputs are read once, so
+# the bytes grow with heads x tokens), for the kernel source with this sha256
+# prefix; None once the source has changed.
+TRAFFIC = {"sha256_prefix": "e2d4f9b187cf8dc4", "bytes": 918.5e6}
 
 
 def peaks():
