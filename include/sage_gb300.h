@@ -189,6 +189,22 @@ sage_status sage_attn_fwd_scores_dump(const int8_t *q_codes, const float *q_scal
                                       void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_attn_fwd_fault_test - exercises the failure detection of
+ * sage_attn_fwd: the same launch, except that the kernel's load warp issues
+ * no copies, so the other warps' bounded waits run out after wait_limit_ns.
+ * Every CTA then stops its loops, frees its tensor memory and returns; the
+ * kernel sets *status_dev to SAGE_ERR_TIMEOUT.  Nothing faults, traps or
+ * hangs, and the CUDA context stays usable.  The output is not written.
+ * status_dev must not be NULL; wait_limit_ns > 0.  Test hook only.
+ * ---------------------------------------------------------------------- */
+sage_status sage_attn_fwd_fault_test(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                                     const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                                     int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
+                                     float sm_scale, void *out_bf16, sage_strides os, void *workspace,
+                                     size_t workspace_bytes, int32_t *status_dev, uint64_t wait_limit_ns,
+                                     void *stream);
+
+/* ------------------------------------------------------------------------
  * int8kv_prompt_attn - causal prompt attention of bf16 queries over an int8
  * KV cache with per-token fp16 scales, grouped-query heads.
  *

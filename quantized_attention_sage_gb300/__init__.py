@@ -22,11 +22,12 @@ from .build import LIB, build as _build_lib
 
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
-    "int8kv_prompt_attn", "sage_attention", "Strides", "STATUS",
+    "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "sage_attention",
+    "Strides", "STATUS",
 ]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
-          4: "workspace too small", 5: "bounded device wait timed out"}
+          4: "workspace too small", 5: "bounded device wait timed out", 6: "problem too large"}
 D = 128
 
 
@@ -81,6 +82,9 @@ def lib():
     L.sage_attn_fwd_scores_dump.restype = i32
     L.sage_attn_fwd_scores_dump.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                             vp, Strides, vp, sz, vp, vp, vp]
+    L.sage_attn_fwd_fault_test.restype = i32
+    L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+                                           vp, Strides, vp, sz, vp, C.c_uint64, vp]
     L.int8kv_prompt_attn_workspace.restype = sz
     L.int8kv_prompt_attn_workspace.argtypes = [i32, i32, i32, i32]
     L.int8kv_prompt_attn.restype = i32
@@ -216,6 +220,30 @@ def sage_attn_fwd_scores_dump(qk: dict, vq: dict, q_block: int = 64, k_block: in
                                        k_block, float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes,
                                        None, _ptr(scores), _stream(stream)), "sage_attn_fwd_scores_dump")
     return out, scores
+
+
+def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: int = 64, k_block: int = 64,
+                             stream=None) -> int:
+    """Launch sage_attn_fwd with its load warp silenced, so every bounded wait runs out.
+
+    Returns the device status word after synchronising (SAGE_ERR_TIMEOUT when the
+    failure detection works).  Test hook: the output is not written."""
+    torch = _torch()
+    qc, kc = qk["q_codes"], qk["k_codes"]
+    B, H, Nq, _ = qc.shape
+    Nk = kc.shape[2]
+    dev = qc.device
+    out = torch.zeros((B, H, Nq, D), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    L = lib()
+    nbytes = L.sage_attn_fwd_workspace(B, H, Nq, Nk)
+    ws = _workspace(nbytes, dev)
+    _check(L.sage_attn_fwd_fault_test(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
+                                      _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block,
+                                      k_block, 0.0, _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
+                                      int(wait_limit_ns), _stream(stream)), "sage_attn_fwd_fault_test")
+    torch.cuda.synchronize(dev)
+    return int(status.item())
 
 
 def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,

@@ -150,7 +150,8 @@ static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, c
                                  const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
                                  int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
                                  sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
-                                 int32_t *s_dump, void *stream) {
+                                 int32_t *s_dump, void *stream, int fault = 0,
+                                 uint64_t wait_ns = 2000000000ull) {
   if (d != kD) return SAGE_ERR_UNSUPPORTED;
   if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
   if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
@@ -180,6 +181,8 @@ static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, c
   a.k_img = ws + size_t(B) * H * Nq * kD * 2;
   a.status = status_dev;
   a.s_dump = s_dump;
+  a.fault = fault;
+  a.wait_ns = wait_ns;
   return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -203,6 +206,17 @@ sage_status sage_attn_fwd_scores_dump(const int8_t *q_codes, const float *q_scal
 }
 
 
+
+sage_status sage_attn_fwd_fault_test(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                                     const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B,
+                                     int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale,
+                                     void *out_bf16, sage_strides os, void *workspace, size_t workspace_bytes,
+                                     int32_t *status_dev, uint64_t wait_limit_ns, void *stream) {
+  if (status_dev == nullptr || wait_limit_ns == 0) return SAGE_ERR_INVALID_ARG;
+  return attn_fwd_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, B, H, Nq, Nk, d, q_block, k_block,
+                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, nullptr, stream, 1,
+                       wait_limit_ns);
+}
 
 size_t int8kv_prompt_attn_workspace(int Nq, int Hq, int Hkv, int Nk) {
   if (Nq < 1 || Hq < 1 || Hkv < 1 || Nk < 1 || Hq % Hkv != 0) return 0;

@@ -69,6 +69,8 @@ struct Params {
   int32_t *status;
   int32_t *s_dump;  // diagnostic: exact scores [B*H][Nq_pad][Nk_pad], or null
   int nq_pad, nk_pad;
+  uint64_t wait_ns;  // limit of every bounded wait
+  int fault;         // test hook: 1 = the producer issues no loads, so waits run out
 };
 
 struct Bars {
@@ -130,46 +132,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (uniform values); one elected lane issues.
     const bool leader = elect_one();
-    if (leader) {
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(&bars->q_full, ntile * kQBytes);
-      for (int t = 0; t < ntile; ++t) {
-        uint8_t *sQ = smem + kOffQ + t * kQBytes;
-        tma_load_3d(sQ, &tmQ, &bars->q_full, 0, q0 + t * BM, bh);
-        tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0 + t * BM, bh);
-      }
-    }
-    __syncwarp();
-    auto load_k = [&](int j) -> bool {
-      const int s = j % NSK;
-      if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
+    // Test hook (fault == 1): issue nothing, so that the consumers' bounded
+    // waits run out and the kernel reports SAGE_ERR_TIMEOUT with no copy in
+    // flight.
+    if (p.fault != 1) {
       if (leader) {
-        uint8_t *dst = smem + kOffK + s * kKBytes;
-        mbar_arrive_expect_tx(&bars->k_full[s], kKBytes);
-        tma_load_3d(dst, &tmK, &bars->k_full[s], 0, j * BN, bh);
-        tma_load_3d(dst + kKBytes / 2, &tmK, &bars->k_full[s], 64, j * BN, bh);
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        mbar_arrive_expect_tx(&bars->q_full, ntile * kQBytes);
+        for (int t = 0; t < ntile; ++t) {
+          uint8_t *sQ = smem + kOffQ + t * kQBytes;
+          tma_load_3d(sQ, &tmQ, &bars->q_full, 0, q0 + t * BM, bh);
+          tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0 + t * BM, bh);
+        }
       }
       __syncwarp();
-      return true;
-    };
-    auto load_v = [&](int j) -> bool {
-      const int s = j % NSV;
-      if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
-      if (leader) {
-        mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
-        tma_load_3d(smem + kOffV + s * kVBytes, &tmV, &bars->v_full[s], j * BN, 0, bh);
+      auto load_k = [&](int j) -> bool {
+        const int s = j % NSK;
+        if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort, p.wait_ns)) return false;
+        if (leader) {
+          uint8_t *dst = smem + kOffK + s * kKBytes;
+          mbar_arrive_expect_tx(&bars->k_full[s], kKBytes);
+          tma_load_3d(dst, &tmK, &bars->k_full[s], 0, j * BN, bh);
+          tma_load_3d(dst + kKBytes / 2, &tmK, &bars->k_full[s], 64, j * BN, bh);
+        }
+        __syncwarp();
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = j % NSV;
+        if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort, p.wait_ns)) return false;
+        if (leader) {
+          mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
+          tma_load_3d(smem + kOffV + s * kVBytes, &tmV, &bars->v_full[s], j * BN, 0, bh);
+        }
+        __syncwarp();
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = load_k(0);
-    for (int j = 0; ok && j < T; ++j) {
-      if (j + 1 < T) ok = load_k(j + 1);
-      if (ok) ok = load_v(j);
+      if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
     }
-    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the event loop (uniform values); one elected lane
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    bool ok = mbar_wait(&bars->q_full, 0, abort) && mbar_wait(&bars->k_full[0], 0, abort);
+    bool ok = mbar_wait(&bars->q_full, 0, abort, p.wait_ns) && mbar_wait(&bars->k_full[0], 0, abort, p.wait_ns);
     if (ok) {
       tc_fence_after();
       for (int t = 0; t < ntile; ++t) issue_qk(t, 0);
@@ -250,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nanosleep(32);  // leave issue slots to the softmax warps of this sub-partition
         const uint64_t now = globaltimer();
         if (idle_since == 0) idle_since = now;
-        else if (now - idle_since > kWaitLimitNs || *abort) ok = false;
+        else if (now - idle_since > p.wait_ns || *abort) ok = false;
       }
     }
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
@@ -281,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float t_lo, t_hi;
       tile_t(0, t_lo, t_hi);
       for (int j = 0; j < T; ++j) {
-        ok = mbar_wait(&bars->s_full[t], j & 1, abort);
+        ok = mbar_wait(&bars->s_full[t], j & 1, abort, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         uint32_t S[128];
@@ -353,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
         // PV_t(j-1) must be complete: it read P_t and accumulated into O_t
         if (j >= 1) {
-          ok = mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort);
+          ok = mbar_wait(&bars->pv_done[t], (j - 1) & 1, abort, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
         }
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         t_lo = nt_lo;
         t_hi = nt_hi;
       }
-      if (ok) ok = mbar_wait(&bars->pv_done[t], (T - 1) & 1, abort);
+      if (ok) ok = mbar_wait(&bars->pv_done[t], (T - 1) & 1, abort, p.wait_ns);
       if (!ok) {
         report(p.status, SAGE_ERR_TIMEOUT);
       } else {
@@ -518,6 +525,8 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.s_dump = a.s_dump;
   p.nq_pad = ceil_div(a.Nq, 2 * BM) * 2 * BM;
   p.nk_pad = npad;
+  p.wait_ns = a.wait_ns;
+  p.fault = a.fault;
 
   static bool attr_set = false;
   if (!attr_set) {

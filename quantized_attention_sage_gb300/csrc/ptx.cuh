@@ -80,16 +80,17 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parit
 }
 
 // Wait for the phase with the given parity to complete.  Gives up when
-// *abort is set by another thread or after kWaitLimitNs; on its own timeout
-// it sets *abort and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// *abort is set by another thread or after limit_ns; on its own timeout it
+// sets *abort and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
     if ((i & 7u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }
