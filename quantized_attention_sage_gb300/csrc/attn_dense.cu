@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -313,50 +315,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[t]);
         float *Sf = reinterpret_cast<float *>(S);
-        const bool masked = nvalid < BN;
-        if (masked) {
-#pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i >= nvalid) Sf[i] = -INFINITY;
-        }
-        // row maximum of the raw scores, four independent chains
-        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
-        float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
-#pragma unroll
-        for (int i = 3; i < 31; i += 2) {
-          c0 = fmax3(c0, Sf[i], Sf[i + 1]);
-          c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
-          c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
-          c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
-        }
-        const float mlo = fmax3(c0, c1, Sf[31]) , mhi = fmax3(c2, c3, Sf[95]);
-        const float mlo2 = fmax3(mlo, Sf[63], Sf[63]), mhi2 = fmax3(mhi, Sf[127], Sf[127]);
-        const float mt = fmaxf(mlo2 == -INFINITY ? -INFINITY : __fmul_rn(mlo2, t_lo),
-                               mhi2 == -INFINITY ? -INFINITY : __fmul_rn(mhi2, t_hi));
-        const float mnew = fmaxf(m, mt);
-        const float alpha = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, mnew));
-        // x = S * t - (m' - log2 448): 2^x = 448 * p
-        const float nb = __fsub_rn(kLog2_448, mnew);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        float mnew, alpha, rowsum;
         uint32_t pk[32];
+        // The tile's softmax; kMasked (keys past Nk in this tile) is a
+        // compile-time flag so that full tiles carry no per-element predicates.
+        auto softmax_tile = [&](auto masked_c) {
+          constexpr bool kMasked = decltype(masked_c)::value;
+          if (kMasked) {
 #pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          const float tt = i < 64 ? t_lo : t_hi;
-          float2 x01 = ffma2(make_float2(Sf[i], Sf[i + 1]), make_float2(tt, tt), make_float2(nb, nb));
-          float2 x23 = ffma2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(tt, tt), make_float2(nb, nb));
-          if (masked) {  // keys past Nk: p = 0 (also when t = 0, where -inf * 0 would be NaN)
-            if (i >= nvalid) x01.x = -INFINITY;
-            if (i + 1 >= nvalid) x01.y = -INFINITY;
-            if (i + 2 >= nvalid) x23.x = -INFINITY;
-            if (i + 3 >= nvalid) x23.y = -INFINITY;
+            for (int i = 0; i < 128; ++i)
+              if (i >= nvalid) Sf[i] = -INFINITY;
           }
-          const float2 q01 = make_float2(ex2(x01.x), ex2(x01.y));
-          const float2 q23 = make_float2(ex2(x23.x), ex2(x23.y));
-          acc0 = fadd2(acc0, q01);
-          acc1 = fadd2(acc1, q23);
-          pk[i >> 2] = __byte_perm(cvt_e4m3x2(q01.x, q01.y), cvt_e4m3x2(q23.x, q23.y), 0x5410);
-        }
-        const float rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+          // row maximum of the raw scores, four independent chains
+          float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
+          float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
+#pragma unroll
+          for (int i = 3; i < 31; i += 2) {
+            c0 = fmax3(c0, Sf[i], Sf[i + 1]);
+            c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
+            c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
+            c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
+          }
+          const float mlo = fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]);
+          const float mhi = fmax3(fmax3(c2, c3, Sf[95]), Sf[127], Sf[127]);
+          float mt;
+          if (kMasked) {
+            mt = fmaxf(mlo == -INFINITY ? -INFINITY : __fmul_rn(mlo, t_lo),
+                       mhi == -INFINITY ? -INFINITY : __fmul_rn(mhi, t_hi));
+          } else {
+            mt = fmaxf(__fmul_rn(mlo, t_lo), __fmul_rn(mhi, t_hi));
+          }
+          mnew = fmaxf(m, mt);
+          alpha = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, mnew));
+          // x = S * t - (m' - log2 448): 2^x = 448 * p
+          const float nb = __fsub_rn(kLog2_448, mnew);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 128; i += 4) {
+            const float tt = i < 64 ? t_lo : t_hi;
+            float2 x01 = ffma2(make_float2(Sf[i], Sf[i + 1]), make_float2(tt, tt), make_float2(nb, nb));
+            float2 x23 = ffma2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(tt, tt), make_float2(nb, nb));
+            if (kMasked) {  // keys past Nk: p = 0 (also when t = 0, where -inf * 0 would be NaN)
+              if (i >= nvalid) x01.x = -INFINITY;
+              if (i + 1 >= nvalid) x01.y = -INFINITY;
+              if (i + 2 >= nvalid) x23.x = -INFINITY;
+              if (i + 3 >= nvalid) x23.y = -INFINITY;
+            }
+            const float2 q01 = make_float2(ex2(x01.x), ex2(x01.y));
+            const float2 q23 = make_float2(ex2(x23.x), ex2(x23.y));
+            acc0 = fadd2(acc0, q01);
+            acc1 = fadd2(acc1, q23);
+            pk[i >> 2] = __byte_perm(cvt_e4m3x2(q01.x, q01.y), cvt_e4m3x2(q23.x, q23.y), 0x5410);
+          }
+          rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+        };
+        if (nvalid < BN) softmax_tile(std::true_type{});
+        else softmax_tile(std::false_type{});
         l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
         // PV_t(j-1) must be complete: it read P_t and accumulated into O_t
         if (j >= 1) {
