@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nvalid = min(BN, p.Nk - j * BN);
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
-        tmem_ld_wait();
+        tmem_ld_wait(S);
         if (p.s_dump != nullptr) {  // diagnostic copy of the exact integer scores
           int32_t *d = p.s_dump + (int64_t(bh) * p.nq_pad + (q0 + t * BM + r)) * p.nk_pad + j * BN;
 #pragma unroll
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(colO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
           tmem_ld32(colO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
           tmem_ld32(colO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
-          tmem_ld_wait();
+          tmem_ld_wait(o);
           const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
           for (int i = 0; i < 128; i += 2) {
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(colO + 32 * c, o);
-          tmem_ld_wait();
+          tmem_ld_wait(o);
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {

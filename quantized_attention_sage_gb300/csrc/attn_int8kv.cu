@@ -27,13 +27,15 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace sg {
 namespace kv {
 
-constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
+constexpr int BM = 128, BN = 128, NSK = 2, NSV = 3;
 constexpr int kThreads = 256;
 constexpr uint32_t kQBytes = BM * kD * 2;
 constexpr uint32_t kKTile = BN * kD * 2;                // bf16 K image
@@ -41,7 +43,10 @@ constexpr uint32_t kVBytes = kD * BN * 2;               // fp16 V^T image
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
 constexpr uint32_t kOffV = kOffK + NSK * kKTile;
-constexpr uint32_t kOffBar = kOffV + NSV * kVBytes;
+// the tile's kt and vs (128 fp32 each) ride with its V tile
+constexpr uint32_t kOffKt = kOffV + NSV * kVBytes;
+constexpr uint32_t kOffVs = kOffKt + NSV * BN * 4;
+constexpr uint32_t kOffBar = kOffVs + NSV * BN * 4;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
@@ -65,7 +70,12 @@ struct Params {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  uint64_t s_full[2], p_full, pv_done;
+  // p_full and pv_done per S/P buffer (tile j uses j & 1).  A softmax warp
+  // may finish tile j+1 before another warp finishes tile j (never two tiles,
+  // since QK(j+2) follows PV(j)), so one barrier per kind could be completed
+  // by the wrong tile's arrivals, and a parity wait on it could be answered
+  // by a phase two behind.
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -109,8 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->s_full[0], 1);
     mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->pv_done, 1);
+    mbar_init(&bars->p_full[0], 4);
+    mbar_init(&bars->p_full[1], 4);
+    mbar_init(&bars->pv_done[0], 1);
+    mbar_init(&bars->pv_done[1], 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -160,9 +172,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         const int key0 = (tb + j) * BN;
         uint8_t *dst = smem + kOffV + s * kVBytes;
-        mbar_arrive_expect_tx(&bars->v_full[s], kVBytes);
+        mbar_arrive_expect_tx(&bars->v_full[s], kVBytes + 2 * BN * 4);
         tma_load_3d(dst, &tmV, &bars->v_full[s], key0, 0, g);
         tma_load_3d(dst + kVBytes / 2, &tmV, &bars->v_full[s], key0 + 64, 0, g);
+        const int64_t row = int64_t(g) * p.Npad + key0;
+        bulk_load(smem + kOffKt + s * BN * 4, p.kt + row, BN * 4, &bars->v_full[s]);
+        bulk_load(smem + kOffVs + s * BN * 4, p.vs + row, BN * 4, &bars->v_full[s]);
       }
       __syncwarp();
       return true;
@@ -201,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0) && (T < 2 || issue_qk(1));
     for (int j = 0; ok && j < T; ++j) {
       const int s = j % NSV;
-      ok = mbar_wait(&bars->p_full, j & 1, abort) && mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
+      ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort) && mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
       if (!ok) break;
       tc_fence_after();
       const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
@@ -216,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (j > 0) || (hl > 0) || (k > 0));
           }
         }
-        tc_commit(&bars->pv_done);
+        tc_commit(&bars->pv_done[j & 1]);
         tc_commit(&bars->v_empty[s]);
       }
       __syncwarp();
@@ -231,12 +246,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = (il < p.QT) && (qi < p.Nq);
     const int pos = p.q_pos0 + qi;  // keys 0..pos are visible
     const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
-    // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16
+    // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16.  The
+    // factor 2^-E is taken into the exponent (p' = 2^(s - m - E)), so the row
+    // sum is l * 2^-E as well and O / l is unchanged.
     const float vmax = __uint_as_float(*p.vmax_bits);
     const int E = vmax > 0.f ? int((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
-    const float wscale = __uint_as_float(uint32_t(127 - E) << 23);  // 2^-E
-    const float *kt_row = p.kt + int64_t(g) * p.Npad;
-    const float *vs_row = p.vs + int64_t(g) * p.Npad;
+    const float Ef = float(E);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
@@ -250,71 +265,102 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
       tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
       const int key0 = (tb + j) * BN;
-      const float *kt = kt_row + key0;
-      const float *vsc = vs_row + key0;
       const int nvis = min(BN, pos - key0 + 1);  // visible keys of this tile (<= 0: none)
-      tmem_ld_wait();
+      // kt and vs of this tile arrived with V(j); its slot is reused only
+      // after PV(j), which waits for this warp's p_full
+      const int sv = j % NSV;
+      ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
+      if (!ok) break;
+      const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4);
+      const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4);
+      tmem_ld_wait(S);
       float *Sf = reinterpret_cast<float *>(S);
-      // s = S * kt (base-2 logits), masked past the query's position
-      float mt = -INFINITY;
+      float mnew, alpha, rowsum;
+      // The tile's softmax; kMasked (some row of the warp sees only part of
+      // the tile) is a compile-time flag so that the tiles below the diagonal
+      // carry no per-element predicates.
+      auto softmax_tile = [&](auto masked_c) {
+        constexpr bool kMasked = decltype(masked_c)::value;
+        // s = S * kt (base-2 logits)
 #pragma unroll
-      for (int i = 0; i < 128; i += 4) {
-        const float4 k4 = __ldg(reinterpret_cast<const float4 *>(kt + i));
-        Sf[i] = __fmul_rn(Sf[i], k4.x);
-        Sf[i + 1] = __fmul_rn(Sf[i + 1], k4.y);
-        Sf[i + 2] = __fmul_rn(Sf[i + 2], k4.z);
-        Sf[i + 3] = __fmul_rn(Sf[i + 3], k4.w);
-      }
-      if (nvis < BN) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= nvis) Sf[i] = -INFINITY;
-      }
-#pragma unroll
-      for (int i = 0; i < 128; i += 2) mt = fmax3(mt, Sf[i], Sf[i + 1]);
-      const float mnew = fmaxf(m, mt);
-      const float alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
-      const float msub = (mnew == -INFINITY) ? 0.f : mnew;
-      // p = 2^(s - m'), row sum, w = p * vs * 2^-E split into fp16 hi + lo,
-      // written over this S buffer: hi at columns 0-63, lo at 64-127
-      float rowsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 v4 = __ldg(reinterpret_cast<const float4 *>(vsc + 32 * c + i));
-          const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
-          float w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float pe = ex2(__fsub_rn(Sf[32 * c + i + u], msub));
-            rowsum = __fadd_rn(rowsum, pe);
-            w[u] = __fmul_rn(pe, __fmul_rn(vv[u], wscale));
-          }
-#pragma unroll
-          for (int u = 0; u < 4; u += 2) {
-            const __half2 h = __floats2half2_rn(w[u], w[u + 1]);
-            const float2 hf = __half22float2(h);
-            const __half2 lw = __floats2half2_rn(__fsub_rn(w[u], hf.x), __fsub_rn(w[u + 1], hf.y));
-            hi[(i + u) >> 1] = *reinterpret_cast<const uint32_t *>(&h);
-            lo[(i + u) >> 1] = *reinterpret_cast<const uint32_t *>(&lw);
-          }
+        for (int i = 0; i < 128; i += 4) {
+          const float4 k4 = kt4[i >> 2];
+          const float2 a = fmul2(make_float2(Sf[i], Sf[i + 1]), make_float2(k4.x, k4.y));
+          const float2 b = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
+          Sf[i] = a.x;
+          Sf[i + 1] = a.y;
+          Sf[i + 2] = b.x;
+          Sf[i + 3] = b.y;
         }
-        tmem_st16(sa + 16 * c, hi);
-        tmem_st16(sa + 64 + 16 * c, lo);
-      }
+        if (kMasked) {  // keys past the query's position
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= nvis) Sf[i] = -INFINITY;
+        }
+        // row maximum, four independent chains
+        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
+        float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
+#pragma unroll
+        for (int i = 3; i < 31; i += 2) {
+          c0 = fmax3(c0, Sf[i], Sf[i + 1]);
+          c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
+          c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
+          c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
+        }
+        const float mt = fmaxf(fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]),
+                               fmax3(fmax3(c2, c3, Sf[95]), Sf[127], Sf[127]));
+        mnew = fmaxf(m, mt);
+        alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
+        // x = s - (m' + E); masked entries stay -inf (p' = 0)
+        const float nb = (mnew == -INFINITY) ? 0.f : __fadd_rn(mnew, Ef);
+        const float2 nb2 = make_float2(nb, nb);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        // p' = 2^x, row sum, w = p' * vs split into fp16 hi + lo, written over
+        // this S buffer: hi at columns 0-63, lo at 64-127
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const int e = 32 * c + i;
+            const float4 v4 = vs4[e >> 2];
+            const float2 x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
+            const float2 x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
+            const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+            const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+            acc0 = fadd2(acc0, p01);
+            acc1 = fadd2(acc1, p23);
+            const float2 w01 = fmul2(p01, make_float2(v4.x, v4.y));
+            const float2 w23 = fmul2(p23, make_float2(v4.z, v4.w));
+            const __half2 h01 = __floats2half2_rn(w01.x, w01.y);
+            const __half2 h23 = __floats2half2_rn(w23.x, w23.y);
+            const float2 r01 = fsub2(w01, __half22float2(h01));
+            const float2 r23 = fsub2(w23, __half22float2(h23));
+            const __half2 l01 = __floats2half2_rn(r01.x, r01.y);
+            const __half2 l23 = __floats2half2_rn(r23.x, r23.y);
+            hi[i >> 1] = *reinterpret_cast<const uint32_t *>(&h01);
+            hi[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+            lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
+            lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+          }
+          tmem_st16(sa + 16 * c, hi);
+          tmem_st16(sa + 64 + 16 * c, lo);
+        }
+        rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+      };
+      if (__any_sync(0xffffffffu, nvis < BN)) softmax_tile(std::true_type{});
+      else softmax_tile(std::false_type{});
       l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
       // O is stable once PV(j-1) is complete; rescale it when the max grew
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = mbar_wait(&bars->pv_done, (j - 1) & 1, abort);
+        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(lane_base + kColO + 32 * c, o);
-          tmem_ld_wait();
+          tmem_ld_wait(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
           tmem_st32(lane_base + kColO + 32 * c, o);
@@ -323,10 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
       m = mnew;
     }
-    if (ok) ok = mbar_wait(&bars->pv_done, (T - 1) & 1, abort);
+    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
     if (!ok) {
       report(p.status, SAGE_ERR_TIMEOUT);
     } else {
@@ -336,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_base + kColO + 32 * c, o);
-        tmem_ld_wait();
+        tmem_ld_wait(o);
         if (valid) {
 #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -432,7 +478,7 @@ __global__ void zero_word_kernel(uint32_t *w) { *w = 0u; }
 // bf16 output.  One warp per row, 4 channels per lane.
 __global__ void __launch_bounds__(256) int8kv_combine_kernel(const float *__restrict__ part_o,
                                                              const float2 *__restrict__ part_ml,
-                                                             const uint32_t *__restrict__ vmax_bits, int Nq, int Hq,
+                                                             int Nq, int Hq,
                                                              int G, int QT, int nqt, int nsplit,
                                                              __nv_bfloat16 *__restrict__ out, int64_t o_tok,
                                                              int64_t o_head) {
@@ -458,10 +504,8 @@ __global__ void __launch_bounds__(256) int8kv_combine_kernel(const float *__rest
     acc.z = __fadd_rn(acc.z, __fmul_rn(wgt, o.z));
     acc.w = __fadd_rn(acc.w, __fmul_rn(wgt, o.w));
   }
-  const float vmax = __uint_as_float(*vmax_bits);
-  const int E = vmax > 0.f ? ((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
-  const float back = __uint_as_float(uint32_t(127 + E) << 23);  // 2^E
-  const float inv = __fdiv_rn(back, L);
+  // O and l both carry the factor 2^-E of the weights
+  const float inv = __fdiv_rn(1.f, L);
   const __nv_bfloat162 a = __floats2bfloat162_rn(__fmul_rn(acc.x, inv), __fmul_rn(acc.y, inv));
   const __nv_bfloat162 b = __floats2bfloat162_rn(__fmul_rn(acc.z, inv), __fmul_rn(acc.w, inv));
   uint2 packed;
@@ -584,7 +628,7 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = a.Nq * a.Hq;
-  int8kv_combine_kernel<<<ceil_div(rows, 8), 256, 0, st>>>(po, pml, vmax, a.Nq, a.Hq, L.G, L.QT, L.nqt, L.nsplit,
+  int8kv_combine_kernel<<<ceil_div(rows, 8), 256, 0, st>>>(po, pml, a.Nq, a.Hq, L.G, L.QT, L.nqt, L.nsplit,
                                                           static_cast<__nv_bfloat16 *>(a.out), a.o_tok, a.o_head);
   return cudaGetLastError();
 }

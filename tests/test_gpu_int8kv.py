@@ -56,6 +56,26 @@ def test_int8kv_matches_oracle_all_rows(cuda_lib, w):
     assert_output_close(got, ref_b, w.name)
 
 
+# Mid-size cases whose query tiles fill the GPU without split-KV, so one CTA
+# walks 16-40 key tiles and every shared-memory ring wraps many times.
+LONG = [
+    synth.Int8KVWorkload("kv_long_g4", 9, 1024, 4096, 32, 8, sub=6),
+    synth.Int8KVWorkload("kv_long_g8_outliers", 9, 640, 5000, 64, 8, 0.01, sub=7),
+]
+
+
+@pytest.mark.parametrize("w", LONG, ids=lambda w: w.name)
+def test_int8kv_long_key_range_sampled(cuda_lib, w):
+    x = synth.int8kv_inputs(w)
+    out = run(cuda_lib, w, x)
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([rng.integers(0, w.Nq, 60), [0, w.Nq - 1]])
+    heads = np.concatenate([rng.integers(0, w.Hq, 60), [0, w.Hq - 1]])
+    ref_b, _ = oracle_bf16(w, x, rows, heads)
+    got = bf16_to_f64(out[torch.as_tensor(rows).cuda(), torch.as_tensor(heads).cuda()])
+    assert_output_close(got, ref_b, w.name)
+
+
 @pytest.mark.parametrize("name", ["prompt32k_q1024", "prompt64k_q512_outliers"])
 def test_int8kv_full_size_sampled(cuda_lib, name):
     w = synth.int8kv_workload(name)
