@@ -15,21 +15,24 @@
 //  * Q, K (fp16 images) and V^T (E4M3) tiles arrive by TMA into 128-byte
 //    swizzled shared memory; S (double-buffered) and O live in TMEM.
 //  * One CTA owns two 128-row query tiles of one (b, h); every K/V tile read
-//    serves both.  Warp 0 issues TMA, warp 1 issues MMAs and owns TMEM,
-//    warps 4-7 and 8-11 are two softmax warpgroups, one per query tile, one
-//    query row per thread (TMEM lane = row).  TMEM: S0, S1, O0, O1, 128
-//    columns each.
-//  * S_t is free as soon as the softmax has loaded it into registers, so the
-//    MMA warp issues QK_t(j+1) right then (barrier s_free): the next scores
-//    are computed while the softmax of the current tile runs, and the
-//    softmax warps never wait for S after the first tile.  P_t (E4M3) goes to
-//    a 128-byte-swizzled shared tile per query tile, read by PV_t(j).
-//  * The MMA warp is event-driven: it polls the barriers of both query tiles
-//    and issues whichever QK or PV is ready, keeping per-tile order.
+//    serves both.  Warp 0 issues TMA; warps 1 and 3 issue Q.K^T of tile 0
+//    and tile 1, warp 2 issues both P.V (tcgen05.mma issue blocks for about
+//    one MMA's execution and slows the softmax warps of the issuing
+//    sub-partition, so the issue is spread); warps 4-7 and 8-11 are two
+//    softmax warpgroups, one per query tile, one query row per thread (TMEM
+//    lane = row).  TMEM: S0, S1, O0, O1, 128 columns each.  The role
+//    warpgroup hands registers to the softmax warpgroups (setmaxnreg).
+//  * S_t is free as soon as the softmax has loaded it into registers, so
+//    QK_t(j+1) is issued right then (barrier s_free): the next scores are
+//    computed while the softmax of the current tile runs.  P_t (E4M3) goes
+//    to a 128-byte-swizzled shared tile per query tile, read by PV_t(j).
+//  * The two softmax warps of a sub-partition take turns for the arithmetic
+//    (one computes while the other loads S, stores P or rescales O).
 //  * Softmax per element: row max on the raw int32-valued S (the dequant
 //    multiplier is positive, so max(fl(S*t)) = fl(max(S)*t)), one FFMA for
 //    S*t - m' + log2(448), ex2 on MUFU (448*p directly), fp32 row sums of
-//    448*p, E4M3 conversion of 448*p.
+//    448*p, E4M3 conversion of 448*p; the ex2 of one group of keys are
+//    issued between the sums and conversions of the previous group.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -79,6 +82,9 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  // turn[t][k]: the softmax warp of tile t in TMEM lane quadrant k may run its
+  // arithmetic (the two tiles' warps of one sub-partition alternate)
+  uint64_t turn[2][4];
   uint32_t tmem_base;
   int abort;
 };
@@ -106,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->k_empty[s], ntile);  // one commit per query tile's Q.K^T
     }
     for (int s = 0; s < NSV; ++s) {
       mbar_init(&bars->v_full[s], 1);
@@ -117,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[t], 4);
       mbar_init(&bars->p_full[t], 4);
       mbar_init(&bars->pv_done[t], 1);
+      for (int k = 0; k < 4; ++k) mbar_init(&bars->turn[t][k], 1);
     }
     bars->abort = 0;
     fence_barrier_init();
@@ -130,6 +137,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Registers: the role warpgroup (warps 0-3) needs few, the softmax arithmetic
+  // schedules better with more.  128 x 48 + 256 x 208 = 59,392 <= 384 x 168,
+  // the registers the CTA was launched with.
+  if (warp < 4) {
+  setmaxnreg_dec<48>();
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (uniform values); one elected lane issues.
@@ -179,91 +191,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the event loop (uniform values); one elected lane
-    // issues the MMAs and commits.
+  } else if (warp <= 3) {
+    // ------------------------------------------------------------ MMA issuers
+    // tcgen05.mma issue blocks for about one MMA's execution time and takes
+    // issue slots from the softmax warps of the issuing warp's sub-partition,
+    // which gate everyone through the barriers.  So the issue is spread over
+    // three sub-partitions, each issuer in a fixed order with blocking waits:
+    // warp 1 issues Q.K^T of tile 0, warp 3 Q.K^T of tile 1, warp 2 both P.V.
+    // A commit tracks the MMAs of its own thread only; the issuers touch
+    // disjoint TMEM columns (S_0, S_1, O_t), and a K stage is released when
+    // both Q.K^T warps' commits have arrived (k_empty counts the tiles).
+    // Each whole warp runs the loop (uniform values); one elected lane issues.
     const bool leader = elect_one();
     // Shared-memory descriptors are built once; a K-step only adds a constant:
     // +32 bytes (2 in the address field) inside a 128-byte swizzle row, +16 KB
     // (1024) to the second 64-column block of an fp16 tile.
-    const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + kOffQ));
-    const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kOffK));
-    const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kOffV));
-    const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kOffP));
     constexpr uint64_t kQStep = kQBytes >> 4, kKStep = kKBytes >> 4, kVStep = kVBytes >> 4, kPStep = kPBytes >> 4;
-    auto issue_qk = [&](int t, int s) {
-      const uint64_t dq = dQ0 + uint64_t(t) * kQStep, dk = dK0 + uint64_t(s) * kKStep;
-      const uint32_t dS = tmem + col_s(t);
-      if (leader) {
-#pragma unroll
-        for (int k = 0; k < kD / 16; ++k) {
-          const uint64_t off = uint64_t((k >> 2) * (kQBytes / 2 / 16) + (k & 3) * 2);
-          umma_f16(dS, dq + off, dk + off, kIdescQK, k > 0);
-        }
-        tc_commit(&bars->s_full[t]);
-      }
-      __syncwarp();
-    };
-    bool ok = mbar_wait(&bars->q_full, 0, abort, p.wait_ns) && mbar_wait(&bars->k_full[0], 0, abort, p.wait_ns);
-    if (ok) {
-      tc_fence_after();
-      for (int t = 0; t < ntile; ++t) issue_qk(t, 0);
-      if (leader) tc_commit(&bars->k_empty[0]);
-      __syncwarp();
-    }
-    // Event loop.  QK_t(j) needs K_j and the softmax's load of S_t(j-1)
-    // (s_free); PV_t(j) needs P_t(j) (p_full) and V_j.  A K or V stage is
-    // released after its last user among the query tiles is issued: with two
-    // tiles, the second user of a stage is the one whose partner already
-    // passed it.
-    int qk0 = 1, qk1 = ntile == 2 ? 1 : T, pv0 = 0, pv1 = ntile == 2 ? 0 : T;
-    uint64_t idle_since = 0;
-    while (ok && (pv0 < T || pv1 < T)) {
-      bool progress = false;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int jq = t ? qk1 : qk0;
-        const int jq_other = t ? qk0 : qk1;
-        if (jq < T && mbar_test(&bars->s_free[t], (jq - 1) & 1) &&
-            mbar_test(&bars->k_full[jq % NSK], (jq / NSK) & 1)) {
+    bool ok = true;
+    if (warp == 1 || warp == 3) {
+      const int t = warp == 1 ? 0 : 1;
+      if (t < ntile) {
+        const uint64_t dq = sdesc_sw128(smem_u32(smem + kOffQ)) + uint64_t(t) * kQStep;
+        const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kOffK));
+        ok = mbar_wait(&bars->q_full, 0, abort, p.wait_ns);
+        for (int j = 0; ok && j < T; ++j) {
+          const int s = j % NSK;
+          ok = mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort, p.wait_ns);
+          // S_t(j) overwrites S_t(j-1): the softmax must have loaded it
+          if (ok && j >= 1) ok = mbar_wait(&bars->s_free[t], (j - 1) & 1, abort, p.wait_ns);
+          if (!ok) break;
           tc_fence_after();
-          issue_qk(t, jq % NSK);
-          if (ntile == 1 || jq_other > jq) {  // last user of K stage jq
-            if (leader) tc_commit(&bars->k_empty[jq % NSK]);
-            __syncwarp();
+          const uint64_t dk = dK0 + uint64_t(s) * kKStep;
+          if (leader) {
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+              const uint64_t off = uint64_t((k >> 2) * (kQBytes / 2 / 16) + (k & 3) * 2);
+              umma_f16(tmem + col_s(t), dq + off, dk + off, kIdescQK, k > 0);
+            }
+            tc_commit(&bars->s_full[t]);
+            tc_commit(&bars->k_empty[s]);
           }
-          if (t) qk1 = jq + 1; else qk0 = jq + 1;
-          progress = true;
+          __syncwarp();
         }
-        const int jp = t ? pv1 : pv0;
-        const int jp_other = t ? pv0 : pv1;
-        if (jp < T && mbar_test(&bars->p_full[t], jp & 1) && mbar_test(&bars->v_full[jp % NSV], (jp / NSV) & 1)) {
+      }
+    } else {
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kOffV));
+      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kOffP));
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % NSV;
+        ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort, p.wait_ns);
+        for (int t = 0; ok && t < ntile; ++t) {
+          ok = mbar_wait(&bars->p_full[t], j & 1, abort, p.wait_ns);
+          if (!ok) break;
           tc_fence_after();
-          const uint64_t dp = dP0 + uint64_t(t) * kPStep, dv = dV0 + uint64_t(jp % NSV) * kVStep;
+          const uint64_t dp = dP0 + uint64_t(t) * kPStep, dv = dV0 + uint64_t(s) * kVStep;
           if (leader) {
 #pragma unroll
             for (int k = 0; k < BN / 32; ++k)
-              umma_f8f6f4(tmem + col_o(t), dp + uint64_t(2 * k), dv + uint64_t(2 * k), kIdescPV, (jp > 0) || (k > 0));
+              umma_f8f6f4(tmem + col_o(t), dp + uint64_t(2 * k), dv + uint64_t(2 * k), kIdescPV, (j > 0) || (k > 0));
             tc_commit(&bars->pv_done[t]);
-            if (ntile == 1 || jp_other > jp) tc_commit(&bars->v_empty[jp % NSV]);
           }
           __syncwarp();
-          if (t) pv1 = jp + 1; else pv0 = jp + 1;
-          progress = true;
         }
-      }
-      if (progress) {
-        idle_since = 0;
-      } else {
-        __nanosleep(32);  // leave issue slots to the softmax warps of this sub-partition
-        const uint64_t now = globaltimer();
-        if (idle_since == 0) idle_since = now;
-        else if (now - idle_since > p.wait_ns || *abort) ok = false;
+        if (ok && leader) tc_commit(&bars->v_empty[s]);
+        __syncwarp();
       }
     }
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
-  } else if (warp >= 4) {
+  }
+  } else {
+    setmaxnreg_inc<208>();
     // ------------------------------------------------------------ softmax / rescale / epilogue
     const int t = (warp - 4) >> 2;  // query tile of this warpgroup
     if (t < ntile) {
@@ -350,27 +347,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           // x = S * t - (m' - log2 448): 2^x = 448 * p
           const float nb = __fsub_rn(kLog2_448, mnew);
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < 128; i += 4) {
+          // Groups of four keys, software-pipelined by hand: the four ex2 of
+          // group g+1 are issued between the sums and E4M3 conversions of
+          // group g (the _ord helpers keep this order), so the MUFU pipe and
+          // the FMA/ALU pipes work side by side.
+          auto group_x = [&](int i, float2 &x01, float2 &x23) {
             const float tt = i < 64 ? t_lo : t_hi;
-            float2 x01 = ffma2(make_float2(Sf[i], Sf[i + 1]), make_float2(tt, tt), make_float2(nb, nb));
-            float2 x23 = ffma2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(tt, tt), make_float2(nb, nb));
+            x01 = ffma2_ord(make_float2(Sf[i], Sf[i + 1]), make_float2(tt, tt), make_float2(nb, nb));
+            x23 = ffma2_ord(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(tt, tt), make_float2(nb, nb));
             if (kMasked) {  // keys past Nk: p = 0 (also when t = 0, where -inf * 0 would be NaN)
               if (i >= nvalid) x01.x = -INFINITY;
               if (i + 1 >= nvalid) x01.y = -INFINITY;
               if (i + 2 >= nvalid) x23.x = -INFINITY;
               if (i + 3 >= nvalid) x23.y = -INFINITY;
             }
-            const float2 q01 = make_float2(ex2(x01.x), ex2(x01.y));
-            const float2 q23 = make_float2(ex2(x23.x), ex2(x23.y));
-            acc0 = fadd2(acc0, q01);
-            acc1 = fadd2(acc1, q23);
-            pk[i >> 2] = __byte_perm(cvt_e4m3x2(q01.x, q01.y), cvt_e4m3x2(q23.x, q23.y), 0x5410);
+          };
+          float2 x01, x23;
+          group_x(0, x01, x23);
+          float2 q01 = make_float2(ex2_ord(x01.x), ex2_ord(x01.y));
+          float2 q23 = make_float2(ex2_ord(x23.x), ex2_ord(x23.y));
+#pragma unroll
+          for (int i = 4; i <= 128; i += 4) {
+            const bool more = i < 128;
+            float2 n01, n23;
+            if (more) group_x(i, n01, n23);
+            float2 r01, r23;
+            if (more) r01.x = ex2_ord(n01.x);
+            acc0 = fadd2_ord(acc0, q01);
+            if (more) r01.y = ex2_ord(n01.y);
+            const uint32_t lo = cvt_e4m3x2_ord(q01.x, q01.y);
+            if (more) r23.x = ex2_ord(n23.x);
+            acc1 = fadd2_ord(acc1, q23);
+            if (more) r23.y = ex2_ord(n23.y);
+            const uint32_t hi = cvt_e4m3x2_ord(q23.x, q23.y);
+            pk[(i - 4) >> 2] = __byte_perm(lo, hi, 0x5410);
+            if (more) {
+              q01 = r01;
+              q23 = r23;
+            }
           }
           rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
         };
+        // The warps of the two tiles that share a sub-partition take turns
+        // for the arithmetic, so that one computes while the other loads S
+        // or waits for its P.V, instead of both competing for issue slots
+        // and then idling together.  Tile 0 goes first in every round.
+        const int quad = warp & 3;
+        if (ntile == 2 && (t == 1 || j >= 1)) {
+          ok = mbar_wait(&bars->turn[t][quad], (t == 1 ? j : j - 1) & 1, abort, p.wait_ns);
+          if (!ok) break;
+        }
         if (nvalid < BN) softmax_tile(std::true_type{});
         else softmax_tile(std::false_type{});
+        if (ntile == 2) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->turn[t ^ 1][quad]);
+        }
         l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
         // PV_t(j-1) must be complete: it read P_t and accumulated into O_t
         if (j >= 1) {

@@ -281,6 +281,48 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Issue-ordered variants (asm volatile keeps their relative order): used to
+// interleave MUFU ex2 with the FMA/ALU work of a neighbouring group, which
+// the compiler's own schedule does not do.
+__device__ __forceinline__ float ex2_ord(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t cvt_e4m3x2_ord(float lo, float hi) {
+  uint16_t r;
+  asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float2 fadd2_ord(float2 a, float2 b) {
+  float2 d;
+  asm volatile("{.reg .b64 ra, rb, rd;\n\t"
+               "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\t"
+               "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0,%1}, rd;}"
+               : "=f"(d.x), "=f"(d.y)
+               : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2_ord(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm volatile("{.reg .b64 ra, rb, rc, rd;\n\t"
+               "mov.b64 ra, {%2,%3};\n\tmov.b64 rb, {%4,%5};\n\tmov.b64 rc, {%6,%7};\n\t"
+               "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0,%1}, rd;}"
+               : "=f"(d.x), "=f"(d.y)
+               : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Two fp32 -> packed E4M3 (round to nearest even, saturate to +-448):
 // `lo` lands in bits 0-7, `hi` in bits 8-15.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
