@@ -332,10 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc1 = fadd2(acc1, p23);
             const float2 w01 = fmul2(p01, make_float2(v4.x, v4.y));
             const float2 w23 = fmul2(p23, make_float2(v4.z, v4.w));
-            const __half2 h01 = __floats2half2_rn(w01.x, w01.y);
-            const __half2 h23 = __floats2half2_rn(w23.x, w23.y);
-            const float2 r01 = fsub2(w01, __half22float2(h01));
-            const float2 r23 = fsub2(w23, __half22float2(h23));
+            // hi = w with its mantissa cut to fp16's 10 bits (exact in fp16
+            // for w >= 2^-14; below that fp16 rounds it, an absolute error
+            // under 2^-25), lo = w - hi exactly in fp32, then rounded to fp16
+            const float2 t01 = make_float2(__uint_as_float(__float_as_uint(w01.x) & 0xFFFFE000u),
+                                           __uint_as_float(__float_as_uint(w01.y) & 0xFFFFE000u));
+            const float2 t23 = make_float2(__uint_as_float(__float_as_uint(w23.x) & 0xFFFFE000u),
+                                           __uint_as_float(__float_as_uint(w23.y) & 0xFFFFE000u));
+            const __half2 h01 = __floats2half2_rn(t01.x, t01.y);
+            const __half2 h23 = __floats2half2_rn(t23.x, t23.y);
+            const float2 r01 = fsub2(w01, t01);
+            const float2 r23 = fsub2(w23, t23);
             const __half2 l01 = __floats2half2_rn(r01.x, r01.y);
             const __half2 l23 = __floats2half2_rn(r23.x, r23.y);
             hi[i >> 1] = *reinterpret_cast<const uint32_t *>(&h01);
