@@ -70,6 +70,8 @@ def lib():
         L.orc_f32_to_e4m3_array.argtypes = [P(f32), i64, P(C.c_uint8)]
         L.orc_e4m3_value_array.argtypes = [P(C.c_uint8), i64, P(f64)]
         L.orc_f16_value_array.argtypes = [P(C.c_uint16), i64, P(f64)]
+        L.orc_f32_to_f16_array.argtypes = [P(f32), i64, P(C.c_uint16)]
+        L.orc_cache_quantise_rows.argtypes = [P(f32), i64, P(C.c_int8), P(C.c_uint16)]
         _lib = L
     return _lib
 
@@ -104,6 +106,25 @@ def f16_value(h) -> np.ndarray:
     out = np.empty(h.shape, dtype=np.float64)
     lib().orc_f16_value_array(_p(h, C.c_uint16), h.size, _p(out, C.c_double))
     return out
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """fp32 -> fp16 bits, round to nearest even (overflow to infinity)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    lib().orc_f32_to_f16_array(_p(x, C.c_float), x.size, _p(out, C.c_uint16))
+    return out
+
+
+def cache_quantise(x) -> tuple[np.ndarray, np.ndarray]:
+    """Per-token int8 KV cache rows: x fp32 [..., 128] -> (int8 codes, fp16 scale bits [...])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    assert x.shape[-1] == 128
+    n = x.size // 128
+    codes = np.empty(x.shape, dtype=np.int8)
+    scales = np.empty(x.shape[:-1], dtype=np.uint16)
+    lib().orc_cache_quantise_rows(_p(x, C.c_float), n, _p(codes, C.c_int8), _p(scales, C.c_uint16))
+    return codes, scales
 
 
 def bf16_value(h) -> np.ndarray:

@@ -99,6 +99,38 @@ double orc_f16_value(uint16_t h)
     return s ? -v : v;
 }
 
+/* fp32 -> fp16, round to nearest even.  Quantum in the binade
+   [2^k, 2^(k+1)) is 2^(k-10) for k >= -14 and 2^-24 below; a magnitude that
+   rounds beyond the largest finite value 65504 becomes infinity, as IEEE
+   round-to-nearest does (the threshold is 65520, halfway to 2^16). */
+uint16_t orc_f32_to_f16(float xf)
+{
+    double x = (double)xf;
+    double a = fabs(x);
+    uint16_t code = 0;
+    if (isnan(x)) {
+        code = 0x7E00u;
+    } else if (a > 0.0) {
+        int e;
+        frexp(a, &e);
+        int k = e - 1;
+        if (k < -14) k = -14;
+        double r = round_to_quantum(a, ldexp(1.0, k - 10));
+        if (r >= 65536.0 || isinf(a)) {
+            code = 0x7C00u;                                     /* infinity */
+        } else if (r < ldexp(1.0, -14)) {
+            code = (uint16_t)(r / ldexp(1.0, -24));              /* subnormal (or 2^-14 exactly below) */
+        } else {
+            double f = frexp(r, &e);                            /* r = f*2^e, f in [0.5, 1) */
+            int E = (e - 1) + 15;
+            int M = (int)((2.0 * f - 1.0) * 1024.0 + 0.5);
+            code = (uint16_t)((E << 10) | M);
+        }
+    }
+    if (signbit(x)) code |= 0x8000u;
+    return code;
+}
+
 /* OCP 8-bit floating point, E4M3 ("FN"): bias 7, 3 mantissa bits, no
    infinities, S.1111.111 is NaN, largest finite 448, subnormals m * 2^-9. */
 double orc_e4m3_value(uint8_t c)
@@ -478,6 +510,34 @@ int orc_int8kv_rows(const uint16_t *q, const int8_t *kc, const uint16_t *ks,
 }
 
 /* ------------------------------------------------------------------------
+ * The int8 KV cache itself, per token: "Strata PR #2092" (int8 K/V cache
+ * with per-token fp16 scales; the cache is written upstream of the prompt
+ * attention).  Reading of the recipe (the page gives the format, not the
+ * rounding): per row of 128 channels of one (kv head, token),
+ *   amax  = max |x_c|                       (exact)
+ *   scale = fp16_rn(fl(amax / 127))         (fp32 division, then fp16)
+ *   code  = clamp(rint_even(fl(x_c / float(scale))), -127, 127), and 0
+ *           wherever the fp16 scale is 0.
+ * x: [nrows][128] fp32; codes [nrows][128]; scales [nrows] fp16 bits.
+ * --------------------------------------------------------------------- */
+void orc_cache_quantise_rows(const float *x, int64_t nrows, int8_t *codes, uint16_t *scales)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const float *row = x + r * D;
+        double amax = 0.0;
+        for (int c = 0; c < D; ++c) {
+            double a = fabs((double)row[c]);
+            if (a > amax) amax = a;
+        }
+        uint16_t h = orc_f32_to_f16((float)FL(amax / 127.0));
+        double s = orc_f16_value(h);
+        scales[r] = h;
+        for (int c = 0; c < D; ++c)
+            codes[r * D + c] = (int8_t)(s > 0.0 ? rni_sat127(FL((double)row[c] / s)) : 0);
+    }
+}
+
+/* ------------------------------------------------------------------------
  * array forms of the conversions (for exhaustive checks from the tests)
  * --------------------------------------------------------------------- */
 void orc_f32_to_bf16_array(const float *x, int64_t n, uint16_t *out)
@@ -498,4 +558,9 @@ void orc_e4m3_value_array(const uint8_t *c, int64_t n, double *out)
 void orc_f16_value_array(const uint16_t *h, int64_t n, double *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f16_value(h[i]);
+}
+
+void orc_f32_to_f16_array(const float *x, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(x[i]);
 }

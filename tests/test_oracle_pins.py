@@ -377,3 +377,76 @@ def test_int8kv_scale_exchange_and_group_sharing():
     o2, _ = oracle.int8kv_rows(q2, x["k"], x["k_scale"], x["v"], x["v_scale"], w.q_pos0,
                                [10, 10], [0, 1], nthreads=1)
     assert np.array_equal(o2[0], o2[1])
+
+
+# ---------------------------------------------------------------------------
+# fp16 encoder and the per-token int8 KV cache quantiser
+# ("Strata PR #2092": int8 K/V cache with per-token fp16 scales)
+# ---------------------------------------------------------------------------
+
+def test_f16_encode_matches_library_rne():
+    rng = np.random.default_rng(21)
+    mant = rng.integers(0, 1 << 23, 400_000).astype(np.uint32)
+    expo = rng.integers(127 - 30, 127 + 17, 400_000).astype(np.uint32)
+    sign = rng.integers(0, 2, 400_000).astype(np.uint32) << 31
+    x = (sign | (expo << 23) | mant).view(np.float32)
+    # exact halfway points between fp16 neighbours (ties), across the subnormal range too
+    h = np.arange(0, 0x7BFF, 7, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    ties = ((lo + hi) / 2).astype(np.float32)
+    edges = np.array([0.0, -0.0, 65504.0, 65519.996, 65520.0, 1e9, 2.0**-24, 2.0**-25, 2.0**-25 * 1.0001,
+                      2.0**-14, 2.0**-14 * (1 - 2.0**-11), np.inf, -np.inf], dtype=np.float32)
+    allx = np.concatenate([x, ties, -ties, edges])
+    with np.errstate(over="ignore"):
+        want = allx.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.f32_to_f16(allx), want)
+
+
+def _cache_rows(seed, n, gain=1.0):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((n, 128)) * gain).astype(np.float32)
+
+
+def test_cache_quantise_properties():
+    x = _cache_rows(5, 3000, gain=np.float32(3.0))
+    x[7] *= 1e-4                      # small row (normal fp16 scale)
+    x[8] *= 1e-9                      # scale below the fp16 subnormal range -> 0
+    codes, sc = oracle.cache_quantise(x)
+    s = oracle.f16_value(sc)
+    amax = np.abs(x.astype(np.float64)).max(axis=1)
+    # the scale is fp16(fl32(amax / 127))
+    assert np.array_equal(sc, oracle.f32_to_f16((x.__abs__().max(axis=1) / np.float32(127.0)).astype(np.float32)))
+    assert np.all(np.abs(codes.astype(np.int32)) <= 127)
+    live = s > 0
+    # the largest element of a row encodes to +-127 (fp16 rounding moves the
+    # scale by at most 2^-11 relative, far less than half a code)
+    arg = np.abs(x).argmax(axis=1)
+    assert np.all(np.abs(codes[np.arange(len(x)), arg][live].astype(np.int32)) == 127)
+    # reconstruction within half a code (plus the scale's own rounding at the top)
+    err = np.abs(x.astype(np.float64) - codes.astype(np.float64) * s[:, None])
+    bound = 0.5 * s[:, None] * (1 + 2.0**-20) + 127 * s[:, None] * 2.0**-11
+    assert np.all(err[live] <= bound[live])
+    # a scale that rounds to 0 gives zero codes
+    assert sc[8] == 0 and not codes[8].any()
+
+
+def test_cache_quantise_zero_row_and_power_of_two():
+    x = _cache_rows(6, 64)
+    x[3] = 0.0
+    codes, sc = oracle.cache_quantise(x)
+    assert sc[3] == 0 and not codes[3].any()
+    for k in (-3, 2, 5):
+        c2, s2 = oracle.cache_quantise(x * np.float32(2.0**k))
+        assert np.array_equal(c2, codes)
+        np.testing.assert_array_equal(oracle.f16_value(s2), oracle.f16_value(sc) * 2.0**k)
+
+
+def test_cache_quantise_agrees_with_the_input_recipe():
+    # the workload generator quantises the synthetic cache with numpy; the
+    # oracle's C quantiser must give the same bits
+    x = _cache_rows(7, 2000, gain=np.float32(0.7))
+    codes, sc = oracle.cache_quantise(x)
+    c2, s2 = synth._cache_quantise(x)
+    assert np.array_equal(codes, c2)
+    assert np.array_equal(sc, s2.view(np.uint16))
