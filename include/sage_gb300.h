@@ -48,6 +48,10 @@ typedef int sage_status;
 #define SAGE_ERR_WORKSPACE 4    /* workspace smaller than the *_workspace() size  */
 #define SAGE_ERR_TIMEOUT 5      /* device side: a bounded wait ran out            */
 #define SAGE_ERR_TOO_LARGE 6    /* beyond the fixed scratch of sage_quantize_qk_noalloc */
+#define SAGE_ERR_NONFINITE 7    /* device side: a non-finite input or scale       */
+
+#define SAGE_DTYPE_BF16 0
+#define SAGE_DTYPE_F32 1
 
 /* Element strides of a [B, H, N, 128] tensor (channel stride is 1). */
 typedef struct {
@@ -235,6 +239,34 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
                                int Hkv, int d, float sm_scale, void *out_bf16, int64_t o_tok_stride,
                                int64_t o_head_stride, void *workspace, size_t workspace_bytes,
                                int32_t *status_dev, void *stream);
+
+/* ------------------------------------------------------------------------
+ * int8kv_cache_write - quantizes N new K and V rows per kv head into the
+ * int8 KV cache read by int8kv_prompt_attn, at cache positions
+ * pos0 .. pos0+N-1.  Page: "Strata PR #2092" (an int8 K/V cache with
+ * per-token fp16 scales, written upstream of the prompt attention).  Per row
+ * of 128 channels of one (kv head, token):
+ *   scale = fp16_rn(fl(amax / 127)),
+ *   code  = clamp(rint_even(fl(x / float(scale))), -127, 127), 0 where the
+ *           fp16 scale is 0.
+ *
+ * k_src, v_src: [N][Hkv][128] with element strides src_tok_stride,
+ *   src_head_stride (channel stride 1), type src_dtype (SAGE_DTYPE_BF16 or
+ *   SAGE_DTYPE_F32); bf16 rows need 8-byte alignment (strides multiples of
+ *   4), fp32 rows 16-byte alignment (strides multiples of 4).
+ * k_cache, v_cache: int8 [Hkv][Ncache][128], head stride cache_head_stride
+ *   elements (>= Ncache*128, a multiple of 16), 16-byte aligned.
+ * k_scale_f16, v_scale_f16: fp16 [Hkv][Ncache], head stride
+ *   scale_head_stride (>= Ncache).
+ * Requires d == 128, N >= 1, Hkv >= 1, 0 <= pos0, pos0 + N <= Ncache.  Only
+ * the N new rows (codes and scales) are written.  If an fp16 scale is not
+ * finite (amax/127 beyond 65504) *status_dev becomes SAGE_ERR_NONFINITE and
+ * that row's codes are undefined.  Inputs must be finite.
+ * ---------------------------------------------------------------------- */
+sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dtype, int64_t src_tok_stride,
+                               int64_t src_head_stride, int N, int Hkv, int d, int pos0, int8_t *k_cache,
+                               int8_t *v_cache, int64_t cache_head_stride, int Ncache, void *k_scale_f16,
+                               void *v_scale_f16, int64_t scale_head_stride, int32_t *status_dev, void *stream);
 
 #ifdef __cplusplus
 }

@@ -22,12 +22,14 @@ from .build import LIB, build as _build_lib
 
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
-    "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "sage_attention",
+    "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
+    "sage_attention",
     "Strides", "STATUS",
 ]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
-          4: "workspace too small", 5: "bounded device wait timed out", 6: "problem too large"}
+          4: "workspace too small", 5: "bounded device wait timed out", 6: "problem too large",
+          7: "non-finite input or scale"}
 D = 128
 
 
@@ -85,6 +87,9 @@ def lib():
     L.sage_attn_fwd_fault_test.restype = i32
     L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                            vp, Strides, vp, sz, vp, C.c_uint64, vp]
+    L.int8kv_cache_write.restype = i32
+    L.int8kv_cache_write.argtypes = [vp, vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i64, i32, vp, vp, i64,
+                                     vp, vp]
     L.int8kv_prompt_attn_workspace.restype = sz
     L.int8kv_prompt_attn_workspace.argtypes = [i32, i32, i32, i32]
     L.int8kv_prompt_attn.restype = i32
@@ -285,6 +290,31 @@ def int8kv_prompt_attn(q, k_cache, k_scale, v_cache, v_scale, q_pos0: int, sm_sc
                                 out.stride(1), _ptr(ws), nbytes, _ptr(status), _stream(stream)),
            "int8kv_prompt_attn")
     return out
+
+
+def int8kv_cache_write(k, v, k_cache, k_scale, v_cache, v_scale, pos0: int, status=None, stream=None):
+    """Quantize new rows k, v [N, Hkv, 128] (bf16 or fp32) into the int8 cache at positions pos0..pos0+N-1.
+
+    k_cache, v_cache: int8 [Hkv, Ncache, 128] (token rows contiguous); k_scale, v_scale: fp16 [Hkv, Ncache]."""
+    torch = _torch()
+    N, Hkv, _ = k.shape
+    if k.dtype != v.dtype or k.stride() != v.stride() or k.stride(2) != 1:
+        raise ValueError("k and v must share dtype and a [N, Hkv, 128] layout with unit channel stride")
+    if k.dtype == torch.bfloat16:
+        dt = 0
+    elif k.dtype == torch.float32:
+        dt = 1
+    else:
+        raise ValueError("k and v must be bf16 or fp32")
+    if k_cache.stride() != v_cache.stride() or k_cache.stride(1) != D or k_cache.stride(2) != 1:
+        raise ValueError("k_cache and v_cache must share a [Hkv, Ncache, 128] layout with contiguous token rows")
+    if k_scale.stride() != v_scale.stride() or k_scale.stride(1) != 1:
+        raise ValueError("k_scale and v_scale must share a [Hkv, Ncache] layout")
+    L = lib()
+    _check(L.int8kv_cache_write(_ptr(k), _ptr(v), dt, k.stride(0), k.stride(1), N, Hkv, D, int(pos0),
+                                _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), k_cache.shape[1], _ptr(k_scale),
+                                _ptr(v_scale), k_scale.stride(0), _ptr(status), _stream(stream)),
+           "int8kv_cache_write")
 
 
 def default_sm_scale() -> float:

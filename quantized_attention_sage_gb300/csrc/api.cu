@@ -77,6 +77,7 @@ const char *sage_status_string(sage_status s) {
     case SAGE_ERR_WORKSPACE: return "workspace too small";
     case SAGE_ERR_TIMEOUT: return "bounded device wait timed out";
     case SAGE_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of the allocation-free entry point";
+    case SAGE_ERR_NONFINITE: return "non-finite input or scale";
     default: return "unknown status";
   }
 }
@@ -263,6 +264,44 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
   a.workspace = workspace;
   a.status = status_dev;
   return from_cuda(launch_int8kv(a, static_cast<cudaStream_t>(stream)));
+}
+
+sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dtype, int64_t src_tok_stride,
+                               int64_t src_head_stride, int N, int Hkv, int d, int pos0, int8_t *k_cache,
+                               int8_t *v_cache, int64_t cache_head_stride, int Ncache, void *k_scale_f16,
+                               void *v_scale_f16, int64_t scale_head_stride, int32_t *status_dev, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if (src_dtype != SAGE_DTYPE_BF16 && src_dtype != SAGE_DTYPE_F32) return SAGE_ERR_UNSUPPORTED;
+  if (N < 1 || Hkv < 1 || pos0 < 0 || Ncache < 1 || int64_t(pos0) + N > Ncache) return SAGE_ERR_INVALID_ARG;
+  const uintptr_t src_align = src_dtype == SAGE_DTYPE_F32 ? 15u : 7u;
+  if (k_src == nullptr || v_src == nullptr || (reinterpret_cast<uintptr_t>(k_src) & src_align) ||
+      (reinterpret_cast<uintptr_t>(v_src) & src_align))
+    return SAGE_ERR_INVALID_ARG;
+  if (src_tok_stride < 0 || src_head_stride < 0 || (src_tok_stride % 4) || (src_head_stride % 4))
+    return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || cache_head_stride < int64_t(Ncache) * kD ||
+      (cache_head_stride % 16))
+    return SAGE_ERR_INVALID_ARG;
+  if (k_scale_f16 == nullptr || v_scale_f16 == nullptr || (reinterpret_cast<uintptr_t>(k_scale_f16) & 1u) ||
+      (reinterpret_cast<uintptr_t>(v_scale_f16) & 1u) || scale_head_stride < Ncache)
+    return SAGE_ERR_INVALID_ARG;
+  CacheWriteArgs a;
+  a.k_src = k_src;
+  a.v_src = v_src;
+  a.src_tok = src_tok_stride;
+  a.src_head = src_head_stride;
+  a.f32 = src_dtype == SAGE_DTYPE_F32;
+  a.N = N;
+  a.Hkv = Hkv;
+  a.pos0 = pos0;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.cache_head = cache_head_stride;
+  a.k_scale = k_scale_f16;
+  a.v_scale = v_scale_f16;
+  a.scale_head = scale_head_stride;
+  a.status = status_dev;
+  return from_cuda(launch_cache_write(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -68,6 +68,20 @@ struct Int8KVArgs {
 size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk);
 cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st);
 
+// int8 KV-cache writer (kvcache.cu)
+struct CacheWriteArgs {
+  const void *k_src, *v_src;  // [N tokens][Hkv heads][128], bf16 or fp32
+  int64_t src_tok, src_head;  // element strides
+  bool f32;
+  int N, Hkv, pos0;
+  int8_t *k_cache, *v_cache;  // [Hkv][Ncache][128]
+  int64_t cache_head;         // element stride between heads
+  void *k_scale, *v_scale;    // fp16 [Hkv][Ncache]
+  int64_t scale_head;
+  int32_t *status;
+};
+cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st);
+
 // tensor-map encoding through the driver entry point (api.cu)
 bool encode_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,

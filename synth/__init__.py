@@ -248,16 +248,30 @@ def int8kv_inputs(w: Int8KVWorkload, kv_heads: tuple[int, int] | None = None) ->
         x = normal_f64(qseed, base, (g1 - g0) * grp * d)
         q[t] = f32_to_bf16_bits(x.astype(np.float32)).reshape((g1 - g0) * grp, d)
     res = {"q": q}
-    for key, tid in (("k", T_K), ("v", T_V)):
-        seed = seed_for(w.config, tid, w.sub)
+    raw = int8kv_raw(w, (g0, g1))
+    for key in ("k", "v"):
         codes = np.empty((g1 - g0, Nk, d), dtype=np.int8)
         scales = np.empty((g1 - g0, Nk), dtype=np.float16)
-        for j, g in enumerate(range(g0, g1)):
-            x = normal_f64(seed, g * Nk * d, Nk * d).astype(np.float32).reshape(Nk, d)
-            if key == "k" and outl.size:
-                chans = outl[(outl // d) == g] % d
-                x[:, chans] *= np.float32(w.outlier_gain)
-            codes[j], scales[j] = _cache_quantise(x)
+        for j in range(g1 - g0):
+            codes[j], scales[j] = _cache_quantise(raw[key][j])
         res[key] = codes
         res[key + "_scale"] = scales
+    return res
+
+
+def int8kv_raw(w: Int8KVWorkload, kv_heads: tuple[int, int] | None = None) -> dict:
+    """The fp32 K/V rows [Hkv, Nk, d] before the cache is quantised (outlier channels applied)."""
+    d, Nk, Hkv = w.d, w.Nk, w.Hkv
+    g0, g1 = (0, Hkv) if kv_heads is None else kv_heads
+    outl = outlier_pairs(w)
+    res = {}
+    for key, tid in (("k", T_K), ("v", T_V)):
+        seed = seed_for(w.config, tid, w.sub)
+        x = np.empty((g1 - g0, Nk, d), dtype=np.float32)
+        for j, g in enumerate(range(g0, g1)):
+            x[j] = normal_f64(seed, g * Nk * d, Nk * d).astype(np.float32).reshape(Nk, d)
+            if key == "k" and outl.size:
+                chans = outl[(outl // d) == g] % d
+                x[j][:, chans] *= np.float32(w.outlier_gain)
+        res[key] = x
     return res

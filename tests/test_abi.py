@@ -110,3 +110,23 @@ def test_int8kv_rejects_bad_arguments(L):
     assert call(kvhs=100) == 1           # kv head stride below Nk * 128
     assert call(q=FAKE + 4) == 1
     assert call(wsb=0) == 4
+
+
+def test_cache_write_rejects_bad_arguments(L):
+    def call(dt=0, N=8, Hkv=2, d=128, pos0=0, Ncache=16, src=FAKE, tok=256, head=128, chs=16 * 128, cache=FAKE,
+             sc=FAKE, schs=16):
+        return L.int8kv_cache_write(src, src, dt, tok, head, N, Hkv, d, pos0, cache, cache, chs, Ncache, sc, sc,
+                                    schs, None, None)
+    assert call(d=64) == 2
+    assert call(dt=5) == 2
+    assert call(pos0=9) == 1              # pos0 + N > Ncache
+    assert call(pos0=-1) == 1
+    assert call(N=0) == 1
+    assert call(chs=100) == 1             # cache head stride below Ncache * 128
+    assert call(schs=8) == 1              # scale head stride below Ncache
+    assert call(src=FAKE + 2) == 1        # bf16 rows need 8-byte alignment
+    assert call(dt=1, src=FAKE + 8) == 1  # fp32 rows need 16-byte alignment
+    assert call(tok=258) == 1             # strides in multiples of 4 elements
+    assert call(cache=FAKE + 8) == 1
+    assert call(sc=FAKE + 1) == 1
+    assert L.sage_status_string(7) != L.sage_status_string(99)
