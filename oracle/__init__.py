@@ -59,9 +59,10 @@ def lib():
         L.orc_quant_v.argtypes = [P(C.c_uint16), i32, i32, P(C.c_uint8), P(f32)]
         L.orc_sage_attn_rows.argtypes = [P(C.c_int8), P(f32), i32, P(C.c_int8), P(f32), i32,
                                          P(C.c_uint8), i32, P(f32), i32, i32, f32, i32,
-                                         P(i32), i32, P(f32), P(C.c_uint16), i32]
+                                         P(i32), i32, P(f32), P(C.c_uint16), i32, i32, P(f64)]
         L.orc_sage_attn_rows.restype = i32
-        L.orc_attn_rows_f64.argtypes = [P(f64), P(f64), P(f64), i32, i32, f64, i32, P(i32), i32, P(f64)]
+        L.orc_attn_rows_f64.argtypes = [P(f64), P(f64), P(f64), i32, i32, f64, i32, P(i32), i32, P(f64),
+                                        i32, P(f64)]
         L.orc_int8kv_rows.argtypes = [P(C.c_uint16), P(C.c_int8), P(C.c_uint16), P(C.c_int8),
                                       P(C.c_uint16), i32, i32, i32, i32, i32, f64,
                                       P(i32), P(i32), i32, P(f64), i32]
@@ -178,10 +179,11 @@ def quant_v(v: np.ndarray):
 
 
 def sage_attn_rows(qc, sq, bq, kc, sk, bk, vct, sv, Nq, Nk, rows=None, sm_scale=SM_SCALE_D128,
-                   tile=128, nthreads=0):
+                   tile=128, nthreads=0, causal=False, with_lse=False):
     """The quantized program for the given query rows of one head.
 
-    Returns (out_f32 [n,128] before rounding, out_bf16 bits [n,128], threads used)."""
+    Returns (out_f32 [n,128] before rounding, out_bf16 bits [n,128], threads used), plus the
+    rows' log-sum-exp (fp64 [n]) when ``with_lse``."""
     rows = np.arange(Nq, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     qc = np.ascontiguousarray(qc, dtype=np.int8)
     kc = np.ascontiguousarray(kc, dtype=np.int8)
@@ -192,15 +194,18 @@ def sage_attn_rows(qc, sq, bq, kc, sk, bk, vct, sv, Nq, Nk, rows=None, sm_scale=
     n = rows.size
     out = np.empty((n, D), dtype=np.float32)
     outb = np.empty((n, D), dtype=np.uint16)
+    lse = np.empty(n, dtype=np.float64)
     used = lib().orc_sage_attn_rows(_p(qc, C.c_int8), _p(sq, C.c_float), bq, _p(kc, C.c_int8),
                                     _p(sk, C.c_float), bk, _p(vct, C.c_uint8), vct.shape[1],
                                     _p(sv, C.c_float), Nq, Nk, float(sm_scale), tile,
                                     _p(rows, C.c_int), n, _p(out, C.c_float), _p(outb, C.c_uint16),
-                                    int(nthreads))
-    return out, outb, used
+                                    int(nthreads), int(bool(causal)),
+                                    _p(lse, C.c_double) if with_lse else None)
+    return (out, outb, used, lse) if with_lse else (out, outb, used)
 
 
-def attn_rows_f64(q, k, v, sm_scale=1.0 / math.sqrt(128.0), tile=128, rows=None):
+def attn_rows_f64(q, k, v, sm_scale=1.0 / math.sqrt(128.0), tile=128, rows=None, causal=False,
+                  with_lse=False):
     """Quantisation-off twin of the same tile loop (fp64, identity quantisers)."""
     q = np.ascontiguousarray(q, dtype=np.float64)
     k = np.ascontiguousarray(k, dtype=np.float64)
@@ -208,20 +213,23 @@ def attn_rows_f64(q, k, v, sm_scale=1.0 / math.sqrt(128.0), tile=128, rows=None)
     Nq, Nk = q.shape[0], k.shape[0]
     rows = np.arange(Nq, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     out = np.empty((rows.size, D), dtype=np.float64)
+    lse = np.empty(rows.size, dtype=np.float64)
     lib().orc_attn_rows_f64(_p(q, C.c_double), _p(k, C.c_double), _p(v, C.c_double), Nq, Nk,
-                            float(sm_scale), tile, _p(rows, C.c_int), rows.size, _p(out, C.c_double))
-    return out
+                            float(sm_scale), tile, _p(rows, C.c_int), rows.size, _p(out, C.c_double),
+                            int(bool(causal)), _p(lse, C.c_double))
+    return (out, lse) if with_lse else out
 
 
-def sage_head(q, k, v, bq, bk, rows=None, sm_scale=SM_SCALE_D128, nthreads=0):
-    """Whole dense path for one head: bf16 bits [N,128] in, everything out."""
+def sage_head(q, k, v, bq, bk, rows=None, sm_scale=SM_SCALE_D128, nthreads=0, causal=False):
+    """Whole dense path for one head: bf16 bits [N,128] in, everything out (incl. the rows' lse)."""
     mu = k_mean(k)
     qc, sq = quant_q(q, bq)
     kc, sk = quant_k(k, bk, mu)
     vct, sv = quant_v(v)
-    out, outb, used = sage_attn_rows(qc, sq, bq, kc, sk, bk, vct, sv, q.shape[0], k.shape[0],
-                                     rows=rows, sm_scale=sm_scale, nthreads=nthreads)
-    return dict(mu=mu, qc=qc, sq=sq, kc=kc, sk=sk, vct=vct, sv=sv, out=out, out_bf16=outb,
+    out, outb, used, lse = sage_attn_rows(qc, sq, bq, kc, sk, bk, vct, sv, q.shape[0], k.shape[0],
+                                          rows=rows, sm_scale=sm_scale, nthreads=nthreads, causal=causal,
+                                          with_lse=True)
+    return dict(mu=mu, qc=qc, sq=sq, kc=kc, sk=sk, vct=vct, sv=sv, out=out, out_bf16=outb, lse=lse,
                 threads=used)
 
 

@@ -310,6 +310,13 @@ void orc_quant_v(const uint16_t *v, int Nk, int Nk_pad, uint8_t *codes_t, float 
  *   O_c   = fl(fl(alpha * O_c) + T_c);  m = m'
  * Epilogue: out_c = fl(fl(O_c / l) * fl(sv_c / 448)).
  * Keys j >= Nk do not exist for the row (their logits are -inf).
+ *
+ * Causal variant (the pages name it as the next step and fix nothing else):
+ * query i sees keys j <= i + (Nk - Nq), the bottom-right alignment under
+ * which the last query sees every key (for Nq = Nk: j <= i); the other
+ * logits are -inf, so a tile with no visible key leaves m, l and O as they
+ * are.  Log-sum-exp of the row, natural base, from the final m and l:
+ * lse = ln 2 * (m + log2 l), evaluated in fp64 (l sums p, not 448 p).
  * --------------------------------------------------------------------- */
 typedef struct {
     int quantized;
@@ -320,8 +327,8 @@ typedef struct {
 
 static void program_row(const orc_prog *pg, const double *qrow, double sq,
                         const double *kmat, const double *skey,
-                        const double *vmat, const double *sv, int Nk,
-                        double *S, double *s, double *P, double *out)
+                        const double *vmat, const double *sv, int Nk, int nvis,
+                        double *S, double *s, double *P, double *out, double *lse)
 {
     double m = -INFINITY, l = 0.0;
     double O[D];
@@ -341,6 +348,7 @@ static void program_row(const orc_prog *pg, const double *qrow, double sq,
             } else {
                 sj = S[j] * pg->C;
             }
+            if (j0 + j >= nvis) sj = -INFINITY;         /* outside the causal window */
             s[j] = sj;
             if (sj > mt) mt = sj;
         }
@@ -375,6 +383,15 @@ static void program_row(const orc_prog *pg, const double *qrow, double sq,
         if (pg->quantized) out[c] = FL(FL(O[c] / l) * FL(sv[c] / pg->pscale));
         else out[c] = O[c] / l * sv[c];
     }
+    if (lse) *lse = log(2.0) * (m + log2(l));
+}
+
+/* visible keys of query row i */
+static int visible_keys(int i, int Nq, int Nk, int causal)
+{
+    if (!causal) return Nk;
+    int v = i + (Nk - Nq) + 1;
+    return v < 0 ? 0 : (v > Nk ? Nk : v);
 }
 
 static int set_threads(int nthreads)
@@ -398,9 +415,8 @@ int orc_sage_attn_rows(const int8_t *qc, const float *sq, int bq,
                        const uint8_t *vct, int Nk_pad, const float *sv,
                        int Nq, int Nk, float sm_scale, int tile,
                        const int *rows, int nrows, float *out_f32, uint16_t *out_bf16,
-                       int nthreads)
+                       int nthreads, int causal, double *lse)
 {
-    (void)Nq;
     int used = set_threads(nthreads);
     double *kmat = (double *)malloc(sizeof(double) * (size_t)Nk * D + 8);
     double *vmat = (double *)malloc(sizeof(double) * (size_t)Nk * D + 8);
@@ -424,7 +440,8 @@ int orc_sage_attn_rows(const int8_t *qc, const float *sq, int bq,
         for (int r = 0; r < nrows; ++r) {
             int i = rows[r];
             for (int c = 0; c < D; ++c) qrow[c] = (double)qc[(size_t)i * D + c];
-            program_row(&pg, qrow, (double)sq[i / bq], kmat, skey, vmat, svd, Nk, S, s, P, out);
+            program_row(&pg, qrow, (double)sq[i / bq], kmat, skey, vmat, svd, Nk,
+                        visible_keys(i, Nq, Nk, causal), S, s, P, out, lse ? lse + r : NULL);
             for (int c = 0; c < D; ++c) {
                 out_f32[(size_t)r * D + c] = (float)out[c];
                 out_bf16[(size_t)r * D + c] = orc_f32_to_bf16((float)out[c]);
@@ -439,9 +456,8 @@ int orc_sage_attn_rows(const int8_t *qc, const float *sq, int bq,
 /* The same tile loop with quantisation off, in fp64: q,k,v [N,128] doubles. */
 void orc_attn_rows_f64(const double *q, const double *k, const double *v,
                        int Nq, int Nk, double sm_scale, int tile,
-                       const int *rows, int nrows, double *out)
+                       const int *rows, int nrows, double *out, int causal, double *lse)
 {
-    (void)Nq;
     double *skey = (double *)malloc(sizeof(double) * (size_t)Nk + 8);
     double sv[D];
     for (int t = 0; t < Nk; ++t) skey[t] = 1.0;
@@ -451,7 +467,9 @@ void orc_attn_rows_f64(const double *q, const double *k, const double *v,
     double *s = (double *)malloc(sizeof(double) * (size_t)tile);
     double *P = (double *)malloc(sizeof(double) * (size_t)tile);
     for (int r = 0; r < nrows; ++r)
-        program_row(&pg, q + (size_t)rows[r] * D, 1.0, k, skey, v, sv, Nk, S, s, P, out + (size_t)r * D);
+        program_row(&pg, q + (size_t)rows[r] * D, 1.0, k, skey, v, sv, Nk,
+                    visible_keys(rows[r], Nq, Nk, causal), S, s, P, out + (size_t)r * D,
+                    lse ? lse + r : NULL);
     free(S); free(s); free(P); free(skey);
 }
 

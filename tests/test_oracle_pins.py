@@ -450,3 +450,75 @@ def test_cache_quantise_agrees_with_the_input_recipe():
     c2, s2 = synth._cache_quantise(x)
     assert np.array_equal(codes, c2)
     assert np.array_equal(sc, s2.view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# causal window and log-sum-exp of the dense program
+# ---------------------------------------------------------------------------
+
+def _bruteforce_causal(q, k, v, sm_scale, off):
+    """fp64 causal softmax(q k^T * sm_scale) v with query i seeing keys j <= i + off; and lse."""
+    s = (q @ k.T) * sm_scale
+    n_q, n_k = s.shape
+    mask = np.arange(n_k)[None, :] > (np.arange(n_q)[:, None] + off)
+    s = np.where(mask, -np.inf, s)
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    return (e @ v) / e.sum(axis=1, keepdims=True), (m[:, 0] + np.log(e.sum(axis=1)))
+
+
+@pytest.mark.parametrize("nq,nk,tile", [(200, 200, 128), (200, 200, 32), (70, 300, 64), (1, 129, 128)])
+def test_causal_tile_loop_and_lse_equal_bruteforce_when_unquantised(nq, nk, tile):
+    rng = np.random.default_rng(nq * 7 + nk)
+    q, k, v = (rng.standard_normal((n, 128)) for n in (nq, nk, nk))
+    sm = 1.0 / math.sqrt(128.0)
+    out, lse = oracle.attn_rows_f64(q, k, v, sm_scale=sm, tile=tile, causal=True, with_lse=True)
+    want, want_lse = _bruteforce_causal(q, k, v, sm, nk - nq)
+    np.testing.assert_allclose(out, want, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, want_lse, rtol=1e-12, atol=1e-12)
+    # non-causal lse as well
+    _, lse_nc = oracle.attn_rows_f64(q, k, v, sm_scale=sm, tile=tile, causal=False, with_lse=True)
+    _, want_nc = _bruteforce_causal(q, k, v, sm, nk)
+    np.testing.assert_allclose(lse_nc, want_nc, rtol=1e-12, atol=1e-12)
+
+
+def _quantised_head(seed, nq, nk, blk=64):
+    w = synth.DenseWorkload("pin", 9, 1, 1, nq, nk, blk, sub=seed)
+    x = synth.dense_inputs(w)
+    q, k, v = x["q"][0, 0], x["k"][0, 0], x["v"][0, 0]
+    mu = oracle.k_mean(k)
+    qc, sq = oracle.quant_q(q, blk)
+    kc, sk = oracle.quant_k(k, blk, mu)
+    vct, sv = oracle.quant_v(v)
+    return qc, sq, kc, sk, vct, sv
+
+
+@pytest.mark.parametrize("nq,nk", [(150, 150), (40, 230)])
+def test_causal_row_equals_the_program_on_its_visible_prefix(nq, nk):
+    # the masked program on the full key set and the unmasked program on the
+    # row's visible keys only are the same computation: bit-identical
+    qc, sq, kc, sk, vct, sv = _quantised_head(11, nq, nk)
+    rows = np.array([r for r in (0, 1, 63, 64, 65, nq - 1) if r < nq])
+    out, outb, _, lse = oracle.sage_attn_rows(qc, sq, 64, kc, sk, 64, vct, sv, nq, nk, rows=rows, causal=True,
+                                              with_lse=True)
+    for r_i, i in enumerate(rows):
+        nvis = i + (nk - nq) + 1
+        o2, b2, _, l2 = oracle.sage_attn_rows(qc, sq, 64, kc[:nvis], sk, 64, np.ascontiguousarray(vct[:, :nvis]),
+                                              sv, nq, nvis, rows=np.array([i]), with_lse=True)
+        assert np.array_equal(out[r_i], o2[0]) and np.array_equal(outb[r_i], b2[0])
+        assert lse[r_i] == l2[0]
+
+
+def test_causal_first_row_is_the_dequantised_first_v_row_and_its_lse():
+    nq = nk = 90
+    qc, sq, kc, sk, vct, sv = _quantised_head(12, nq, nk)
+    out, outb, _, lse = oracle.sage_attn_rows(qc, sq, 64, kc, sk, 64, vct, sv, nq, nk, rows=np.array([0]),
+                                              causal=True, with_lse=True)
+    # a single visible key: p = 1, P = 448, out = V_0 * sv
+    v0 = oracle.e4m3_value(vct[:, 0]) * sv.astype(np.float64)
+    np.testing.assert_allclose(out[0], v0, rtol=2.0**-22, atol=0)
+    # lse = ln 2 * s_00 with s_00 = fl(S_00 * fl(fl(sq*sk) * C))
+    C = np.float32(oracle.SM_SCALE_D128 * np.float32(1.4426950408889634))
+    t = np.float32(np.float32(sq[0] * sk[0]) * C)
+    s00 = np.float32(np.float32(int(qc[0].astype(np.int64) @ kc[0].astype(np.int64))) * t)
+    assert lse[0] == pytest.approx(math.log(2.0) * float(s00), rel=1e-15)
