@@ -335,6 +335,24 @@ def run_ours(args, rank, world):
     e2e = {"value": whole_job_tflops(w.flops, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
            "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
 
+    # ---- causal dense attention with the row log-sum-exp, same workload and codes
+    for _ in range(3):
+        qas.sage_attn_fwd(qk, vq, bq, bk, out=out, workspace=ws_a, status=status, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    reps_c = max(5, args.steps // 2)
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(reps_c):
+        qas.sage_attn_fwd(qk, vq, bq, bk, out=out, workspace=ws_a, status=status, causal=True, return_lse=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    assert status.item() == 0, "device status set in causal sage_attn_fwd"
+    ms_c = c0.elapsed_time(c1) / reps_c
+    visible = N * (N + 1) // 2  # query i sees keys 0..i
+    causal = {"ms": ms_c, "tflops_visible": 4 * visible * D * H * B / (ms_c * 1e-3) / 1e12,
+              "tflops_formula": w.flops / (ms_c * 1e-3) / 1e12, "lse": True}
+
     # ---- int8 KV-cache prompt attention
     kv = {}
     for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
@@ -363,6 +381,30 @@ def run_ours(args, rank, world):
                     "tflops_causal": 4 * wk.visible_pairs * 128 * wk.Hq / (ms * 1e-3) / 1e12,
                     "Nq": wk.Nq, "Nk": wk.Nk, "Hq": wk.Hq, "Hkv": wk.Hkv}
     assert status.item() == 0, "device status set in int8kv_prompt_attn"
+    # ---- int8 KV-cache writer: the whole 32K cache of the prompt chunk from bf16 rows
+    wk = synth.int8kv_workload("prompt32k_q1024")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(synth.seed_for(wk.config, synth.T_K))
+    kr = torch.randn((wk.Nk, wk.Hkv, 128), generator=gen, device=dev).to(torch.bfloat16)
+    vr = torch.randn((wk.Nk, wk.Hkv, 128), generator=gen, device=dev).to(torch.bfloat16)
+    kc = torch.empty((wk.Hkv, wk.Nk, 128), dtype=torch.int8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((wk.Hkv, wk.Nk), dtype=torch.float16, device=dev)
+    vs = torch.empty_like(ks)
+    for _ in range(3):
+        qas.int8kv_cache_write(kr, vr, kc, ks, vc, vs, 0, status=status)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        qas.int8kv_cache_write(kr, vr, kc, ks, vc, vs, 0, status=status)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    rows = wk.Nk * wk.Hkv
+    nbytes = rows * (2 * 256 + 2 * 128 + 2 * 2)  # bf16 K and V rows in, int8 codes and fp16 scales out
+    kv["cache_write_32k_bf16"] = {"ms": ms, "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                                  "tokens": wk.Nk, "Hkv": wk.Hkv}
+    assert status.item() == 0, "device status set in int8kv_cache_write"
 
     if rank != 0:
         if dist:
@@ -370,6 +412,7 @@ def run_ours(args, rank, world):
         return
 
     pk = peaks()
+    kv["cache_write_32k_bf16"]["frac_hbm"] = kv["cache_write_32k_bf16"]["gbs"] / pk["hbm_gbs"]
     p16 = pk["bf16_tflops"]
     # Q.K^T on the f16 tensor path, P.V on FP8 (2x the f16 rate, nominal ratio):
     # equal FLOPs on both, so the effective peak is the harmonic combination.
@@ -391,6 +434,7 @@ def run_ours(args, rank, world):
                      "peak_note": (f"{pk['source']}: bf16 burst {p16} TFLOP/s for the Q.K^T half, x2 (nominal "
                                    f"fp8/bf16 ratio) for the P.V half")},
         "components": comp,
+        "causal_lse": causal,
         "int8kv": kv,
         "clocks": clocks,
         "e2e": e2e,

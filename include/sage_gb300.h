@@ -177,6 +177,24 @@ sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const in
                           size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_attn_fwd_ex - sage_attn_fwd with two options the pages name as the
+ * next steps of the dense path ("H3 Performance Roadmap", "Phase 4: Dense
+ * Sage-Compatible Attention"): a causal mask and the per-row log-sum-exp.
+ *   causal: 0 or 1.  With 1, query i sees keys j <= i + (Nk - Nq) (the last
+ *           query sees every key; for Nq == Nk, j <= i).  Requires Nq <= Nk,
+ *           else SAGE_ERR_UNSUPPORTED.
+ *   lse:    NULL, or fp32 [B][H][Nq] (contiguous, 4-byte aligned): the natural
+ *           log of sum_j exp(s_ij) over the row's visible keys, s the scaled
+ *           logits sm_scale * q.k of the quantized program.
+ * Everything else as sage_attn_fwd (which equals causal = 0, lse = NULL).
+ * ---------------------------------------------------------------------- */
+sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                             const float *k_scales, const uint8_t *v_codes, const float *v_scales,
+                             int B, int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale,
+                             int causal, void *out_bf16, sage_strides os, float *lse, void *workspace,
+                             size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/* ------------------------------------------------------------------------
  * sage_attn_fwd_scores_dump - sage_attn_fwd that also writes, for checking,
  * every exact integer score S = q_codes . k_codes^T the tensor cores produced
  * for the attention (the Q.K^T of the defining passage above), as int32 into

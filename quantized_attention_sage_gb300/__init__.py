@@ -84,6 +84,9 @@ def lib():
     L.sage_attn_fwd_scores_dump.restype = i32
     L.sage_attn_fwd_scores_dump.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                             vp, Strides, vp, sz, vp, vp, vp]
+    L.sage_attn_fwd_ex.restype = i32
+    L.sage_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                   vp, Strides, vp, vp, sz, vp, vp]
     L.sage_attn_fwd_fault_test.restype = i32
     L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                            vp, Strides, vp, sz, vp, C.c_uint64, vp]
@@ -185,8 +188,12 @@ def sage_quantize_v(v, out=None, workspace=None, stream=None):
 
 
 def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
-                  out=None, workspace=None, status=None, stream=None):
-    """Quantized attention forward over the two quantisers' outputs; bf16 [B,H,Nq,128]."""
+                  out=None, workspace=None, status=None, stream=None, causal: bool = False,
+                  return_lse: bool = False):
+    """Quantized attention forward over the two quantisers' outputs; bf16 [B,H,Nq,128].
+
+    ``causal``: query i sees keys j <= i + (Nk - Nq).  ``return_lse``: also return the
+    rows' natural log-sum-exp, fp32 [B,H,Nq]."""
     torch = _torch()
     qc, kc = qk["q_codes"], qk["k_codes"]
     B, H, Nq, _ = qc.shape
@@ -197,11 +204,18 @@ def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_s
     L = lib()
     nbytes = L.sage_attn_fwd_workspace(B, H, Nq, Nk)
     ws = _workspace(nbytes, dev, workspace)
-    _check(L.sage_attn_fwd(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
-                           _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
-                           float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
-                           _stream(stream)), "sage_attn_fwd")
-    return out
+    if not causal and not return_lse:
+        _check(L.sage_attn_fwd(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
+                               _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
+                               float(sm_scale), _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
+                               _stream(stream)), "sage_attn_fwd")
+        return out
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev) if return_lse else None
+    _check(L.sage_attn_fwd_ex(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
+                              _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
+                              float(sm_scale), int(bool(causal)), _ptr(out), _strides4(out), _ptr(lse), _ptr(ws),
+                              nbytes, _ptr(status), _stream(stream)), "sage_attn_fwd_ex")
+    return (out, lse) if return_lse else out
 
 
 def sage_attn_fwd_scores_dump(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
@@ -252,11 +266,12 @@ def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: in
 
 
 def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,
-                   stream=None):
+                   stream=None, causal: bool = False, return_lse: bool = False):
     """The dense path in one call: quantize Q/K, quantize V, attention."""
     qk = sage_quantize_qk(q, k, q_block, k_block, stream=stream)
     vq = sage_quantize_v(v, stream=stream)
-    return sage_attn_fwd(qk, vq, q_block, k_block, sm_scale, out=out, stream=stream)
+    return sage_attn_fwd(qk, vq, q_block, k_block, sm_scale, out=out, stream=stream, causal=causal,
+                         return_lse=return_lse)
 
 
 # ---------------------------------------------------------------------------

@@ -152,8 +152,11 @@ static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, c
                                  int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, void *out_bf16,
                                  sage_strides os, void *workspace, size_t workspace_bytes, int32_t *status_dev,
                                  int32_t *s_dump, void *stream, int fault = 0,
-                                 uint64_t wait_ns = 2000000000ull) {
+                                 uint64_t wait_ns = 2000000000ull, int causal = 0, float *lse = nullptr) {
   if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SAGE_ERR_INVALID_ARG;
   if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
   if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
   if (!aligned16(q_codes) || !aligned16(k_codes) || !aligned16(v_codes) || q_scales == nullptr ||
@@ -184,7 +187,19 @@ static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, c
   a.s_dump = s_dump;
   a.fault = fault;
   a.wait_ns = wait_ns;
+  a.causal = causal;
+  a.lse = lse;
   return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
+}
+
+sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
+                             const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B, int H,
+                             int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, int causal,
+                             void *out_bf16, sage_strides os, float *lse, void *workspace, size_t workspace_bytes,
+                             int32_t *status_dev, void *stream) {
+  return attn_fwd_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, B, H, Nq, Nk, d, q_block, k_block,
+                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, nullptr, stream, 0,
+                       2000000000ull, causal, lse);
 }
 
 sage_status sage_attn_fwd(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,

@@ -74,6 +74,8 @@ struct Params {
   int32_t *status;
   int32_t *s_dump;  // diagnostic: exact scores [B*H][Nq_pad][Nk_pad], or null
   int nq_pad, nk_pad;
+  int causal;        // query i sees keys j <= i + (Nk - Nq)
+  float *lse;        // per-row log-sum-exp [B*H][Nq] (natural base), or null
   uint64_t wait_ns;  // limit of every bounded wait
   int fault;         // test hook: 1 = the producer issues no loads, so waits run out
 };
@@ -104,9 +106,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * 2 * BM;
+  // causal: the CTAs with the most key tiles (the last query rows) start first
+  const int qpair = p.causal ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
+  const int q0 = qpair * 2 * BM;
   const int ntile = (q0 + BM < p.Nq) ? 2 : 1;  // second query tile present?
-  const int T = ceil_div(p.Nk, BN);
+  const int coff = p.Nk - p.Nq;                 // causal offset: row i sees keys <= i + coff
+  const int T = p.causal ? (min(q0 + ntile * BM, p.Nq) - 1 + coff) / BN + 1 : ceil_div(p.Nk, BN);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -295,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
         tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
         tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
-        const int nvalid = min(BN, p.Nk - j * BN);
+        // keys of this tile that exist and, when causal, that the row may see
+        const int nvalid = p.causal ? min(min(BN, p.Nk - j * BN), row + coff - j * BN + 1) : min(BN, p.Nk - j * BN);
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait(S);
@@ -397,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = mbar_wait(&bars->turn[t][quad], (t == 1 ? j : j - 1) & 1, abort, p.wait_ns);
           if (!ok) break;
         }
-        if (nvalid < BN) softmax_tile(std::true_type{});
+        if (__any_sync(0xffffffffu, nvalid < BN)) softmax_tile(std::true_type{});
         else softmax_tile(std::false_type{});
         if (ntile == 2) {
           __syncwarp();
@@ -471,6 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
           }
         }
+        // log-sum-exp in the natural base: l sums 448 * 2^(s - m)
+        if (p.lse != nullptr && valid)
+          p.lse[int64_t(bh) * p.Nq + row] = (m + (log2f(l) - kLog2_448)) * 0.6931471805599453f;
       }
     }
   }
@@ -571,6 +580,8 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.s_dump = a.s_dump;
   p.nq_pad = ceil_div(a.Nq, 2 * BM) * 2 * BM;
   p.nk_pad = npad;
+  p.causal = a.causal;
+  p.lse = a.lse;
   p.wait_ns = a.wait_ns;
   p.fault = a.fault;
 

@@ -47,6 +47,8 @@ struct DenseArgs {
   int32_t *s_dump = nullptr;  // diagnostic score dump or null
   uint64_t wait_ns = 2000000000ull;  // limit of every bounded wait inside the kernel
   int fault = 0;                     // test hook (see sage_attn_fwd_fault_test)
+  int causal = 0;                    // query i sees keys j <= i + (Nk - Nq)
+  float *lse = nullptr;              // per-row log-sum-exp [B*H][Nq], or null
 };
 size_t dense_workspace_bytes(int B, int H, int Nq, int Nk);
 cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st);

@@ -31,3 +31,22 @@ def assert_output_close(got: np.ndarray, ref: np.ndarray, what: str):
     max_abs, rel = errors(got, ref)
     assert max_abs <= MAX_ABS and rel <= REL_L2, f"{what}: max-abs {max_abs:.3e}, rel-L2 {rel:.3e}"
     return max_abs, rel
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |x| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def assert_output_close_rows(got: np.ndarray, ref: np.ndarray, what: str):
+    """The bar for outputs whose rows may average only a few keys (causal rows near
+    the start): rel-L2 <= 1e-3 as always, and every element within max-abs 2e-3 or
+    one bf16 step of the oracle's value, whichever is larger.  A row that sees one
+    or two keys has outputs of order one, where a single bf16 rounding that falls
+    the other way (fp32 sums in another order) is already 2^-8 or 2^-7."""
+    max_abs, rel = errors(got, ref)
+    bound = np.maximum(MAX_ABS, bf16_ulp(ref))
+    worst = float(np.max(np.abs(got - ref) / bound)) if got.size else 0.0
+    assert rel <= REL_L2 and worst <= 1.0, f"{what}: rel-L2 {rel:.3e}, max-abs {max_abs:.3e}, worst/bound {worst:.2f}"
+    return max_abs, rel

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_output_close, bf16_dev, bf16_to_f64, bits_to_f64, errors
+from gpu_helpers import assert_output_close, assert_output_close_rows, bf16_dev, bf16_to_f64, bits_to_f64, errors
 
 pytestmark = pytest.mark.gpu
 
@@ -139,3 +139,91 @@ def test_dense_int32_scores_are_exact(cuda_lib, name):
         got = scores[0, h, :w.Nq, :w.Nk].cpu().numpy().astype(np.int64)
         assert np.array_equal(got, exact), f"{name} h{h}"
         assert np.abs(exact).max() <= 128 * 127 * 127
+
+
+def check_lse(lse_gpu: torch.Tensor, lse_ref: np.ndarray, what: str):
+    """Row log-sum-exp: both sides take the same running max m; the sums differ
+    only by fp32 summation order and the GPU's ex2, so 1e-5 absolute + relative."""
+    got = lse_gpu.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got)), what
+    err = np.abs(got - lse_ref)
+    bound = 1e-5 * (1.0 + np.abs(lse_ref))
+    assert np.all(err <= bound), f"{what}: lse error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("nq,nk,bq,bk", [(257, 257, 64, 64), (100, 300, 128, 64), (1, 513, 64, 64),
+                                         (600, 600, 128, 128), (383, 700, 64, 128), (129, 129, 128, 64)])
+def test_dense_causal_with_lse_matches_oracle(cuda_lib, nq, nk, bq, bk):
+    """Causal (query i sees keys j <= i + Nk - Nq) with the row log-sum-exp, against
+    the oracle's causal program: codes bit-exact, outputs and lse within the bar."""
+    w = synth.DenseWorkload(f"causal_{nq}_{nk}", 9, 1, 3, nq, nk, 64, sub=(nq * 5 + nk) % 89)
+    x = synth.dense_inputs(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), bq, bk)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    out, lse = cuda_lib.sage_attn_fwd(qk, vq, bq, bk, status=status, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for h in range(w.H):
+        ref = oracle.sage_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], bq, bk, causal=True)
+        assert np.array_equal(qk["q_codes"][0, h].cpu().numpy(), ref["qc"])
+        assert np.array_equal(qk["k_codes"][0, h].cpu().numpy(), ref["kc"])
+        assert_output_close_rows(bf16_to_f64(out[0, h]), bits_to_f64(ref["out_bf16"]), f"causal {nq}x{nk} h{h} out")
+        check_lse(lse[0, h], ref["lse"], f"causal {nq}x{nk} h{h}")
+
+
+@pytest.mark.parametrize("name", ["sweep_b1h4n65", "sweep_b1h4n257", "tiny_b1h2n256"])
+def test_dense_lse_non_causal(cuda_lib, name):
+    """return_lse without the mask: the same output bits as the plain call, and the
+    oracle's log-sum-exp."""
+    w = synth.dense_workload(name)
+    x = synth.dense_inputs(w)
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), w.block, w.block)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    out, lse = cuda_lib.sage_attn_fwd(qk, vq, w.block, w.block, return_lse=True)
+    plain = cuda_lib.sage_attn_fwd(qk, vq, w.block, w.block)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), plain.view(torch.int16))
+    for h in range(w.H):
+        ref = oracle.sage_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.block, w.block)
+        check_lse(lse[0, h], ref["lse"], f"{name} h{h}")
+
+
+def test_dense_causal_square_first_row_is_first_v_row(cuda_lib):
+    """Nq = Nk causal: row 0 sees key 0 alone, so its output is the dequantised
+    V row 0 (within one bf16 rounding) and its lse is that key's scaled logit."""
+    w = synth.DenseWorkload("causal_row0", 10, 1, 2, 300, 300, 64)
+    x = synth.dense_inputs(w)
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), 64, 64)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    out, lse = cuda_lib.sage_attn_fwd(qk, vq, 64, 64, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    for h in range(2):
+        vrow = oracle.e4m3_value(vq["v_codes"][0, h, :, 0].cpu().numpy()) * vq["v_scales"][0, h].cpu().numpy()
+        got = bf16_to_f64(out[0, h, 0])
+        assert np.all(np.abs(got - vrow) <= 2.0 ** -8 * np.abs(vrow) + 1e-30)
+        s00 = float(np.dot(qk["q_codes"][0, h, 0].cpu().numpy().astype(np.int64),
+                           qk["k_codes"][0, h, 0].cpu().numpy().astype(np.int64)))
+        logit = s00 * float(qk["q_scales"][0, h, 0]) * float(qk["k_scales"][0, h, 0]) / np.sqrt(128.0)
+        assert abs(float(lse[0, h, 0]) - logit) <= 1e-5 * (1.0 + abs(logit))
+
+
+def test_dense_causal_full_size_videodit_sampled(cuda_lib):
+    """The 37,810-token, 24-head workload with the causal mask; sampled rows of two
+    heads (outputs and lse) against the oracle's causal program."""
+    w = synth.dense_workload("videodit_b1h24n37810")
+    x = synth.dense_inputs(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), w.block, w.block)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    out, lse = cuda_lib.sage_attn_fwd(qk, vq, w.block, w.block, status=status, causal=True, return_lse=True)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    rng = np.random.default_rng(11)
+    for h in (3, 22):
+        rows = np.unique(np.concatenate([rng.integers(0, w.Nq, 40), [0, 1, 255, 256, w.Nq - 1]]))
+        ref = oracle.sage_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.block, w.block, rows=rows, causal=True)
+        got = bf16_to_f64(out[0, h][torch.as_tensor(rows).cuda()])
+        assert_output_close_rows(got, bits_to_f64(ref["out_bf16"]), f"videodit causal h{h}")
+        check_lse(lse[0, h][torch.as_tensor(rows).cuda()], ref["lse"], f"videodit causal h{h}")
