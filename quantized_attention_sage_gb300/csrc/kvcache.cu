@@ -11,8 +11,11 @@
 //
 // GB300 design: HBM-bound streaming.  One warp per row, four channels per
 // lane (8- or 16-byte loads, 4-byte code stores: a row is one 128-byte line
-// of the cache), the row maximum by warp shuffles, a grid-stride loop over
-// rows ordered so that consecutive warps write consecutive cache rows.
+// of the cache), the row maximum by warp shuffles, one division-free code per
+// channel (a multiply by the correctly rounded reciprocal of the scale, with
+// the exact quotient taken only next to a rounding boundary), no 64-bit
+// division in the row loop; one resident grid of 8 blocks of 256 threads per
+// SM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -22,53 +25,80 @@ namespace sg {
 namespace kvc {
 
 template <bool kF32>
+__device__ __forceinline__ void load_row(const void *src, int64_t off, float (&x)[4]) {
+  if (kF32) {
+    const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
+    x[0] = v.x;
+    x[1] = v.y;
+    x[2] = v.z;
+    x[3] = v.w;
+  } else {
+    const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(src) + off);
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  }
+}
+
+// One row of 128 channels held four per lane: fp16 scale and int8 codes.
+// q = x * fl(1/s) is within 3 * 2^-24 * |x/s| of fl(x/s); |x/s| stays below
+// 2 * 127 even for an fp16-subnormal scale, so q and fl(x/s) round to the same
+// integer unless q lies within 1e-4 of a half-integer, where the quotient is
+// divided out with IEEE division.
+__device__ __forceinline__ void encode_row(const float (&x)[4], int lane, int8_t *dst_codes, __half *dst_scale,
+                                           int32_t *status) {
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
+  const float sc = __half2float(s16);
+  uint32_t packed = 0;
+  if (sc > 0.f) {
+    const float inv = __frcp_rn(sc);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float q = __fmul_rn(x[k], inv);
+      float rq = rintf(q);
+      if (0.5f - fabsf(q - rq) < 1e-4f) rq = rintf(__fdiv_rn(x[k], sc));
+      int c = int(rq);
+      c = c > 127 ? 127 : (c < -127 ? -127 : c);
+      packed |= (uint32_t(c) & 0xFFu) << (8 * k);
+    }
+  }
+  *reinterpret_cast<uint32_t *>(dst_codes + 4 * lane) = packed;
+  if (lane == 0) {
+    *dst_scale = s16;
+    if (!(fabsf(sc) <= 65504.f) && status) atomicCAS(status, 0, SAGE_ERR_NONFINITE);
+  }
+}
+
+// Each warp takes a contiguous range of (token, head) pairs, head fastest, so
+// that consecutive rows of the source are read in address order, and encodes
+// the K and the V row of each pair (two loads in flight).
+template <bool kF32>
 __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteArgs a) {
   const int lane = threadIdx.x & 31;
-  const int64_t rows_per = int64_t(a.Hkv) * a.N;  // rows of one tensor
-  const int64_t nrows = 2 * rows_per;
-  const int64_t step = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t row = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; row < nrows; row += step) {
-    const int which = row >= rows_per ? 1 : 0;  // 0: K, 1: V
-    const int64_t rr = row - which * rows_per;
-    const int h = int(rr / a.N), t = int(rr - int64_t(h) * a.N);
-    const int64_t src_off = int64_t(t) * a.src_tok + int64_t(h) * a.src_head + 4 * lane;
-    float x[4];
-    if (kF32) {
-      const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(which ? a.v_src : a.k_src) +
-                                                         src_off);
-      x[0] = v.x;
-      x[1] = v.y;
-      x[2] = v.z;
-      x[3] = v.w;
-    } else {
-      const uint2 w = *reinterpret_cast<const uint2 *>(
-          static_cast<const __nv_bfloat16 *>(which ? a.v_src : a.k_src) + src_off);
-      x[0] = __uint_as_float(w.x << 16);
-      x[1] = __uint_as_float(w.x & 0xFFFF0000u);
-      x[2] = __uint_as_float(w.y << 16);
-      x[3] = __uint_as_float(w.y & 0xFFFF0000u);
-    }
-    float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
-    const float s = __half2float(s16);
-    uint32_t packed = 0;
-    if (s > 0.f) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        int c = __float2int_rn(__fdiv_rn(x[u], s));
-        c = c > 127 ? 127 : (c < -127 ? -127 : c);
-        packed |= (uint32_t(c) & 0xFFu) << (8 * u);
-      }
-    }
+  const int64_t P = int64_t(a.N) * a.Hkv;  // (token, head) pairs, head fastest
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t chunk = (P + nwarps - 1) / nwarps;
+  int64_t p = warp0 * chunk;
+  const int64_t pend = min(P, p + chunk);
+  if (p >= pend) return;
+  int t = int(p / a.Hkv), h = int(p - int64_t(t) * a.Hkv);
+  for (; p < pend; ++p) {
+    const int64_t off = int64_t(t) * a.src_tok + int64_t(h) * a.src_head + 4 * lane;
+    float xk[4], xv[4];
+    load_row<kF32>(a.k_src, off, xk);
+    load_row<kF32>(a.v_src, off, xv);
     const int64_t pos = int64_t(a.pos0) + t;
-    int8_t *cache = which ? a.v_cache : a.k_cache;
-    *reinterpret_cast<uint32_t *>(cache + int64_t(h) * a.cache_head + pos * kD + 4 * lane) = packed;
-    if (lane == 0) {
-      __half *sc = static_cast<__half *>(which ? a.v_scale : a.k_scale);
-      sc[int64_t(h) * a.scale_head + pos] = s16;
-      if (!(fabsf(s) <= 65504.f) && a.status) atomicCAS(a.status, 0, SAGE_ERR_NONFINITE);
+    const int64_t co = int64_t(h) * a.cache_head + pos * kD, so = int64_t(h) * a.scale_head + pos;
+    encode_row(xk, lane, a.k_cache + co, static_cast<__half *>(a.k_scale) + so, a.status);
+    encode_row(xv, lane, a.v_cache + co, static_cast<__half *>(a.v_scale) + so, a.status);
+    if (++h == a.Hkv) {
+      h = 0;
+      ++t;
     }
   }
 }
@@ -80,7 +110,7 @@ cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t nrows = 2 * int64_t(a.Hkv) * a.N;
-  const int64_t want = (nrows + 7) / 8, cap = int64_t(sms) * 16;
+  const int64_t want = (nrows + 7) / 8, cap = int64_t(sms) * 8;
   const int blocks = int(want < cap ? want : cap);
   if (a.f32) kvc::cache_write_kernel<true><<<blocks, 256, 0, st>>>(a);
   else kvc::cache_write_kernel<false><<<blocks, 256, 0, st>>>(a);

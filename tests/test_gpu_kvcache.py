@@ -109,3 +109,31 @@ def test_cache_write_reproduces_the_workload_cache_and_feeds_the_attention(cuda_
                                 heads.ravel())
     ref_b = oracle.bf16_value(oracle.f32_to_bf16(ref.astype(np.float32)))
     assert_output_close(bf16_to_f64(out).reshape(-1, 128), ref_b, w.name)
+
+
+def test_cache_write_codes_at_rounding_boundaries(cuda_lib):
+    """Rows whose quotients x / scale fall exactly on half-integers (ties to even)
+    and one fp32 step either side of them, for scales 1, 1/2, 3/8 and an
+    fp16-subnormal scale: the codes must equal the oracle's IEEE-division codes."""
+    rows = []
+    for amax, s in ((127.0, 1.0), (63.5, 0.5), (47.625, 0.375)):
+        k = np.arange(-126, 127, dtype=np.float64)
+        half = (k + 0.5) * s
+        for x in (half, np.nextafter(half.astype(np.float32), np.float32(np.inf)).astype(np.float64),
+                  np.nextafter(half.astype(np.float32), np.float32(-np.inf)).astype(np.float64)):
+            for start in range(0, x.size, 127):
+                r = np.zeros(128)
+                seg = x[start:start + 127]
+                r[:seg.size] = seg
+                r[127] = amax  # fixes the scale to fp16(amax / 127) = s
+                rows.append(r)
+    # fp16-subnormal scale: amax / 127 below 2^-14
+    tiny = np.zeros(128)
+    tiny[:5] = [1e-6, -7.5e-7, 3.1e-7, 6e-8, -1e-6]
+    rows.append(tiny)
+    x = np.asarray(rows, dtype=np.float32)[:, None, :]          # [N, 1, 128] fp32
+    t = torch.from_numpy(x).cuda()
+    kc, vc, ks, vs, st = _write(cuda_lib, t, t, x.shape[0], 0)
+    assert st == 0
+    _check_rows(x, kc, ks, 0)
+    _check_rows(x, vc, vs, 0)
