@@ -9,9 +9,10 @@
 //   code  = clamp(rint_even(fl(x_c / float(scale))), -127, 127); 0 where the
 //           fp16 scale is 0.
 //
-// GB300 design: HBM-bound streaming.  One warp per row, four channels per
-// lane (8- or 16-byte loads, 4-byte code stores: a row is one 128-byte line
-// of the cache), the row maximum by warp shuffles, one division-free code per
+// GB300 design: HBM-bound streaming.  Rows whose source is 16-byte aligned
+// take a wide kernel (8 lanes per row, four rows per warp); others one warp
+// per row, four channels per lane (8- or 16-byte loads, 4-byte code stores: a
+// row is one 128-byte line of the cache), the row maximum by warp shuffles, one division-free code per
 // channel (a multiply by the correctly rounded reciprocal of the scale, with
 // the exact quotient taken only next to a rounding boundary), no 64-bit
 // division in the row loop; one resident grid of 8 blocks of 256 threads per
@@ -103,6 +104,100 @@ __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteArgs a) {
   }
 }
 
+// Wide variant for 16-byte aligned rows: 8 lanes per row, 16 channels per
+// lane (16-byte loads and code stores), four rows per warp (the K and V rows
+// of two consecutive (token, head) pairs), the row maximum over 16 values and
+// three shuffles: about half the instructions per row of the narrow kernel.
+// The codes follow the same steps as encode_row.
+template <bool kF32>
+__global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a) {
+  const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
+  const int64_t P = int64_t(a.N) * a.Hkv;
+  const int64_t P2 = (P + 1) >> 1;  // pair couples
+  const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t chunk = (P2 + nwarps - 1) / nwarps;
+  int64_t q = warp0 * chunk;
+  const int64_t qend = min(P2, q + chunk);
+  if (q >= qend) return;
+  // this lane's pair: 2q + (grp >> 1); K for even groups, V for odd
+  int64_t p = 2 * q + (grp >> 1);
+  int t = int(p / a.Hkv), h = int(p - int64_t(t) * a.Hkv);
+  const bool isv = grp & 1;
+  const void *src = isv ? a.v_src : a.k_src;
+  int8_t *cache = isv ? a.v_cache : a.k_cache;
+  __half *scale = static_cast<__half *>(isv ? a.v_scale : a.k_scale);
+  for (; q < qend; ++q) {
+    const bool live = p < P;
+    float x[16];
+    if (live) {
+      const int64_t off = int64_t(t) * a.src_tok + int64_t(h) * a.src_head + 16 * l8;
+      if (kF32) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 v = s4[u];
+          x[4 * u] = v.x;
+          x[4 * u + 1] = v.y;
+          x[4 * u + 2] = v.z;
+          x[4 * u + 3] = v.w;
+        }
+      } else {
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 w = s4[u];
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            x[8 * u + 2 * k] = __uint_as_float(ww[k] << 16);
+            x[8 * u + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) x[k] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
+    const float sc = __half2float(s16);
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if (sc > 0.f) {
+      const float inv = __frcp_rn(sc);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float qq = __fmul_rn(x[k], inv);
+        float rq = rintf(qq);
+        if (0.5f - fabsf(qq - rq) < 1e-4f) rq = rintf(__fdiv_rn(x[k], sc));
+        int c = int(rq);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        packed[k >> 2] |= (uint32_t(c) & 0xFFu) << (8 * (k & 3));
+      }
+    }
+    if (live) {
+      const int64_t pos = int64_t(a.pos0) + t;
+      *reinterpret_cast<uint4 *>(cache + int64_t(h) * a.cache_head + pos * kD + 16 * l8) =
+          make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      if (l8 == 0) {
+        scale[int64_t(h) * a.scale_head + pos] = s16;
+        if (!(fabsf(sc) <= 65504.f) && a.status) atomicCAS(a.status, 0, SAGE_ERR_NONFINITE);
+      }
+    }
+    // next couple: pair p + 2
+    p += 2;
+    h += 2;
+    while (h >= a.Hkv) {
+      h -= a.Hkv;
+      ++t;
+    }
+  }
+}
+
 }  // namespace kvc
 
 cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st) {
@@ -112,8 +207,17 @@ cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st) {
   const int64_t nrows = 2 * int64_t(a.Hkv) * a.N;
   const int64_t want = (nrows + 7) / 8, cap = int64_t(sms) * 8;
   const int blocks = int(want < cap ? want : cap);
-  if (a.f32) kvc::cache_write_kernel<true><<<blocks, 256, 0, st>>>(a);
-  else kvc::cache_write_kernel<false><<<blocks, 256, 0, st>>>(a);
+  // 16-byte aligned rows (fp32 rows always are) take the wide kernel
+  const int64_t esz = a.f32 ? 4 : 2;
+  const bool wide = ((reinterpret_cast<uintptr_t>(a.k_src) | reinterpret_cast<uintptr_t>(a.v_src)) & 15u) == 0 &&
+                    (a.src_tok * esz) % 16 == 0 && (a.src_head * esz) % 16 == 0;
+  if (wide) {
+    if (a.f32) kvc::cache_write_wide_kernel<true><<<blocks, 256, 0, st>>>(a);
+    else kvc::cache_write_wide_kernel<false><<<blocks, 256, 0, st>>>(a);
+  } else {
+    if (a.f32) kvc::cache_write_kernel<true><<<blocks, 256, 0, st>>>(a);
+    else kvc::cache_write_kernel<false><<<blocks, 256, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

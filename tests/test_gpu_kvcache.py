@@ -137,3 +137,21 @@ def test_cache_write_codes_at_rounding_boundaries(cuda_lib):
     assert st == 0
     _check_rows(x, kc, ks, 0)
     _check_rows(x, vc, vs, 0)
+
+
+def test_cache_write_bf16_rows_without_16_byte_alignment(cuda_lib):
+    """bf16 rows whose token stride is 4 elements short of a 16-byte multiple take
+    the one-warp-per-row kernel; its codes and scales equal the oracle's too."""
+    N, Hkv, Ncache, pos0 = 93, 3, 120, 9
+    rng = np.random.default_rng(17)
+    x = (rng.standard_normal((2, N, Hkv * 128 + 4)) * rng.uniform(0.05, 20, (2, N, 1))).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    x16 = synth.bf16_bits_to_f32(bits)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    k = t[0].as_strided((N, Hkv, 128), (Hkv * 128 + 4, 128, 1))
+    v = t[1].as_strided((N, Hkv, 128), (Hkv * 128 + 4, 128, 1))
+    assert (k.stride(0) * 2) % 16 == 8
+    kc, vc, ks, vs, st = _write(cuda_lib, k, v, Ncache, pos0)
+    assert st == 0
+    _check_rows(x16[0][:, :Hkv * 128].reshape(N, Hkv, 128), kc, ks, pos0)
+    _check_rows(x16[1][:, :Hkv * 128].reshape(N, Hkv, 128), vc, vs, pos0)
