@@ -195,6 +195,36 @@ sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const
                              size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_attention_host - the dense path (sage_quantize_qk, sage_quantize_v,
+ * sage_attn_fwd_ex) on HOST buffers, with the host<->device copies of one
+ * group of heads overlapped with the kernels of the previous group.  The
+ * (batch, head) problems are independent ("H3 Performance Roadmap", section
+ * "Phase 4: Dense Sage-Compatible Attention": one dense attention per head),
+ * so the B*H heads are cut into chunks of head_chunk; one copy stream moves
+ * chunk c+2 in and chunk c out while the compute stream runs chunk c+1.
+ *   q_host, out_host: bf16 [B][H][Nq][128] contiguous; k_host, v_host: bf16
+ *     [B][H][Nk][128] contiguous.  Page-locked memory lets the copies overlap
+ *     the kernels (pageable memory works, without overlap).
+ *   head_chunk >= 1: heads per chunk (the last chunk may be smaller).
+ *   causal: 0 or 1 as in sage_attn_fwd_ex (no lse here).
+ *   workspace: device memory of sage_attention_host_workspace(B, H, Nq, Nk,
+ *     head_chunk) bytes (double-buffered bf16 chunks, codes, scales and the
+ *     three entry points' workspaces); shared by successive calls.
+ *   compute_stream, copy_stream: two different streams.  Everything is
+ *     enqueued asynchronously; out_host is complete once compute_stream has
+ *     reached the end of the call (it waits for the last copy).  The copies
+ *     start after the work already queued on compute_stream.
+ * Errors as the three entry points; SAGE_ERR_INVALID_ARG for a null pointer,
+ * head_chunk < 1 or equal streams.  After an error, work already enqueued may
+ * still run: synchronise both streams before reusing the buffers.
+ * ---------------------------------------------------------------------- */
+size_t sage_attention_host_workspace(int B, int H, int Nq, int Nk, int head_chunk);
+sage_status sage_attention_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, int B,
+                                int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, int causal,
+                                int head_chunk, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                                void *compute_stream, void *copy_stream);
+
+/* ------------------------------------------------------------------------
  * sage_attn_fwd_scores_dump - sage_attn_fwd that also writes, for checking,
  * every exact integer score S = q_codes . k_codes^T the tensor cores produced
  * for the attention (the Q.K^T of the defining passage above), as int32 into

@@ -23,7 +23,7 @@ from .build import LIB, build as _build_lib
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
     "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
-    "sage_attention",
+    "sage_attention", "sage_attention_host",
     "Strides", "STATUS",
 ]
 
@@ -84,6 +84,11 @@ def lib():
     L.sage_attn_fwd_scores_dump.restype = i32
     L.sage_attn_fwd_scores_dump.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                             vp, Strides, vp, sz, vp, vp, vp]
+    L.sage_attention_host_workspace.restype = sz
+    L.sage_attention_host_workspace.argtypes = [i32, i32, i32, i32, i32]
+    L.sage_attention_host.restype = i32
+    L.sage_attention_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp,
+                                      vp, vp]
     L.sage_attn_fwd_ex.restype = i32
     L.sage_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                    vp, Strides, vp, vp, sz, vp, vp]
@@ -272,6 +277,36 @@ def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: floa
     vq = sage_quantize_v(v, stream=stream)
     return sage_attn_fwd(qk, vq, q_block, k_block, sm_scale, out=out, stream=stream, causal=causal,
                          return_lse=return_lse)
+
+
+_copy_streams = {}
+
+
+def sage_attention_host(q, k, v, out, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
+                        causal: bool = False, head_chunk: int = 4, workspace=None, status=None, stream=None,
+                        copy_stream=None):
+    """The dense path on host tensors q, out [B,H,Nq,128] and k, v [B,H,Nk,128] (bf16, contiguous;
+    page-locked for the copies to overlap the kernels).  Groups of ``head_chunk`` heads are copied
+    in on ``copy_stream`` while the previous group is computed on ``stream``; ``out`` is complete once
+    ``stream`` reaches the end of the call.  Both streams must differ (non-default streams overlap)."""
+    torch = _torch()
+    for t in (q, k, v, out):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("q, k, v, out must be contiguous bf16 [B, H, N, 128] host tensors")
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if copy_stream is None:
+        copy_stream = _copy_streams.get(dev.index)
+        if copy_stream is None:
+            copy_stream = _copy_streams[dev.index] = torch.cuda.Stream(device=dev)
+    L = lib()
+    nbytes = L.sage_attention_host_workspace(B, H, Nq, Nk, head_chunk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_attention_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Nq, Nk, D, q_block, k_block,
+                                 float(sm_scale), int(bool(causal)), int(head_chunk), _ptr(ws), nbytes,
+                                 _ptr(status), _stream(stream), _stream(copy_stream)), "sage_attention_host")
+    return out
 
 
 # ---------------------------------------------------------------------------

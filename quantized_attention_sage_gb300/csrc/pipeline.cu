@@ -1,0 +1,185 @@
+// sage_attention_host: the dense path on host-resident Q, K, V and output,
+// with the host<->device copies overlapped with the kernels.
+//
+// The (batch, head) problems are independent, so the heads are cut into
+// chunks.  One copy stream moves chunk c+2's inputs in and chunk c's output
+// out while the compute stream quantizes and attends chunk c+1; inputs and
+// outputs are double-buffered in the caller's workspace, the intermediates
+// (codes, scales, fp16 images) are single-buffered because only the compute
+// stream touches them.  Cross-stream order comes from events created for the
+// call (timing disabled) and released as soon as they are enqueued.
+//
+// Per chunk c (slot s = c % 2):
+//   copy:    H2D q, k, v -> in[s]          record in_ready[c]
+//   compute: wait in_ready[c]; quantize Q/K, quantize V, attention
+//            -> out[s]                     record done[c]
+//   copy:    wait done[c]; D2H out[s]; then H2D of chunk c+2 into in[s]
+// H2D(c+2) follows done[c] (in[s] has been read) and D2H(c) on the copy
+// stream, so compute(c+2), which waits for in_ready[c+2], also finds out[s]
+// drained.  The copy stream first waits for the work already queued on the
+// compute stream; at the end the compute stream waits for the last D2H, so
+// the caller synchronises one stream.
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct HostLayout {
+  int hc;                                  // heads per chunk
+  size_t q_bytes, k_bytes, o_bytes;        // bf16 chunk buffers
+  size_t off_in[2][3], off_out[2];         // double-buffered inputs (q, k, v) and output
+  size_t off_qc, off_kc, off_qs, off_ks, off_mu, off_vc, off_vs, off_wqk, off_wv, off_wa;
+  size_t wqk, wv, wa, total;
+};
+
+HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
+  HostLayout L{};
+  const int BH = B * H;
+  L.hc = head_chunk < BH ? head_chunk : BH;
+  const size_t hc = size_t(L.hc);
+  L.q_bytes = hc * Nq * sg::kD * 2;
+  L.k_bytes = hc * Nk * sg::kD * 2;
+  L.o_bytes = L.q_bytes;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += up(bytes);
+    return o;
+  };
+  for (int s = 0; s < 2; ++s) {
+    L.off_in[s][0] = take(L.q_bytes);
+    L.off_in[s][1] = take(L.k_bytes);
+    L.off_in[s][2] = take(L.k_bytes);
+    L.off_out[s] = take(L.o_bytes);
+  }
+  L.off_qc = take(hc * Nq * sg::kD);
+  L.off_kc = take(hc * Nk * sg::kD);
+  L.off_qs = take(hc * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
+  L.off_ks = take(hc * sg::ceil_div(Nk, 64) * sizeof(float));
+  L.off_mu = take(hc * sg::kD * sizeof(float));
+  L.off_vc = take(hc * sg::kD * size_t(sg::nk_pad(Nk)));
+  L.off_vs = take(hc * sg::kD * sizeof(float));
+  L.wqk = sage_quantize_qk_workspace(1, L.hc, Nk);
+  L.wv = sage_quantize_v_workspace(1, L.hc, Nk);
+  L.wa = sage_attn_fwd_workspace(1, L.hc, Nq, Nk);
+  L.off_wqk = take(L.wqk);
+  L.off_wv = take(L.wv);
+  L.off_wa = take(L.wa);
+  L.total = off + kAlign;  // room to align the base
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sage_attention_host_workspace(int B, int H, int Nq, int Nk, int head_chunk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || head_chunk < 1) return 0;
+  return host_layout(B, H, Nq, Nk, head_chunk).total;
+}
+
+sage_status sage_attention_host(const void *q_host, const void *k_host, const void *v_host, void *out_host, int B,
+                                int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale, int causal,
+                                int head_chunk, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                                void *compute_stream, void *copy_stream) {
+  if (d != sg::kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || head_chunk < 1 || int64_t(B) * H > 65535 || Nq > (1 << 28) ||
+      Nk > (1 << 28))
+    return SAGE_ERR_INVALID_ARG;
+  if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || workspace == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  if (copy_stream == nullptr || copy_stream == compute_stream) return SAGE_ERR_INVALID_ARG;
+  const HostLayout L = host_layout(B, H, Nq, Nk, head_chunk);
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + kAlign - 1) &
+                                            ~uintptr_t(kAlign - 1));
+  cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), xs = static_cast<cudaStream_t>(copy_stream);
+
+  const int BH = B * H;
+  const int C = sg::ceil_div(BH, L.hc);
+  std::vector<cudaEvent_t> in_ready(C, nullptr), done(C, nullptr);
+  cudaEvent_t start = nullptr, last = nullptr;
+  sage_status st = SAGE_OK;
+  auto fail = [&](sage_status s) {
+    if (st == SAGE_OK) st = s;
+  };
+  auto ck = [&](cudaError_t e) {
+    if (e != cudaSuccess) fail(SAGE_ERR_CUDA);
+    return e == cudaSuccess;
+  };
+  for (int c = 0; c < C && st == SAGE_OK; ++c) {
+    ck(cudaEventCreateWithFlags(&in_ready[c], cudaEventDisableTiming));
+    ck(cudaEventCreateWithFlags(&done[c], cudaEventDisableTiming));
+  }
+  if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&last, cudaEventDisableTiming));
+  if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&start, cudaEventDisableTiming));
+  // the copies start after everything already queued on the compute stream
+  // (e.g. a previous call that used the same workspace)
+  if (st == SAGE_OK && ck(cudaEventRecord(start, cs))) ck(cudaStreamWaitEvent(xs, start, 0));
+
+  const size_t qrow = size_t(Nq) * sg::kD * 2, krow = size_t(Nk) * sg::kD * 2;  // bytes per head
+  auto heads_of = [&](int c) { return (c + 1) * L.hc <= BH ? L.hc : BH - c * L.hc; };
+  auto h2d = [&](int c) {
+    const int s = c & 1, n = heads_of(c);
+    const size_t h0 = size_t(c) * L.hc;
+    ck(cudaMemcpyAsync(ws + L.off_in[s][0], static_cast<const uint8_t *>(q_host) + h0 * qrow, n * qrow,
+                       cudaMemcpyHostToDevice, xs));
+    ck(cudaMemcpyAsync(ws + L.off_in[s][1], static_cast<const uint8_t *>(k_host) + h0 * krow, n * krow,
+                       cudaMemcpyHostToDevice, xs));
+    ck(cudaMemcpyAsync(ws + L.off_in[s][2], static_cast<const uint8_t *>(v_host) + h0 * krow, n * krow,
+                       cudaMemcpyHostToDevice, xs));
+    ck(cudaEventRecord(in_ready[c], xs));
+  };
+  if (st == SAGE_OK) h2d(0);
+  if (st == SAGE_OK && C > 1) h2d(1);
+  for (int c = 0; c < C && st == SAGE_OK; ++c) {
+    const int s = c & 1, n = heads_of(c);
+    if (!ck(cudaStreamWaitEvent(cs, in_ready[c], 0))) break;
+    const sage_strides qs{int64_t(n) * Nq * sg::kD, int64_t(Nq) * sg::kD, sg::kD};
+    const sage_strides kvs{int64_t(n) * Nk * sg::kD, int64_t(Nk) * sg::kD, sg::kD};
+    auto *qc = reinterpret_cast<int8_t *>(ws + L.off_qc);
+    auto *kc = reinterpret_cast<int8_t *>(ws + L.off_kc);
+    auto *qsc = reinterpret_cast<float *>(ws + L.off_qs);
+    auto *ksc = reinterpret_cast<float *>(ws + L.off_ks);
+    auto *vc = reinterpret_cast<uint8_t *>(ws + L.off_vc);
+    auto *vsc = reinterpret_cast<float *>(ws + L.off_vs);
+    sage_status r = sage_quantize_qk(ws + L.off_in[s][0], qs, ws + L.off_in[s][1], kvs, 1, n, Nq, Nk, sg::kD,
+                                     q_block, k_block, qc, qsc, kc, ksc, reinterpret_cast<float *>(ws + L.off_mu),
+                                     ws + L.off_wqk, L.wqk, cs);
+    if (r == SAGE_OK)
+      r = sage_quantize_v(ws + L.off_in[s][2], kvs, 1, n, Nk, sg::kD, vc, vsc, ws + L.off_wv, L.wv, cs);
+    if (r == SAGE_OK)
+      r = sage_attn_fwd_ex(qc, qsc, kc, ksc, vc, vsc, 1, n, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal,
+                           ws + L.off_out[s], qs, nullptr, ws + L.off_wa, L.wa, status_dev, cs);
+    if (r != SAGE_OK) {
+      fail(r);
+      break;
+    }
+    if (!ck(cudaEventRecord(done[c], cs))) break;
+    if (!ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
+    ck(cudaMemcpyAsync(static_cast<uint8_t *>(out_host) + size_t(c) * L.hc * qrow, ws + L.off_out[s], n * qrow,
+                       cudaMemcpyDeviceToHost, xs));
+    if (c + 2 < C) h2d(c + 2);
+  }
+  if (st == SAGE_OK && ck(cudaEventRecord(last, xs))) ck(cudaStreamWaitEvent(cs, last, 0));
+  // events still pending on the device are released once they complete
+  for (int c = 0; c < C; ++c) {
+    if (in_ready[c]) cudaEventDestroy(in_ready[c]);
+    if (done[c]) cudaEventDestroy(done[c]);
+  }
+  if (last) cudaEventDestroy(last);
+  if (start) cudaEventDestroy(start);
+  return st;
+}
+
+}  // extern "C"

@@ -130,3 +130,22 @@ def test_cache_write_rejects_bad_arguments(L):
     assert call(cache=FAKE + 8) == 1
     assert call(sc=FAKE + 1) == 1
     assert L.sage_status_string(7) != L.sage_status_string(99)
+
+
+def test_host_pipeline_rejects_bad_arguments(L):
+    ws = L.sage_attention_host_workspace(1, 4, 256, 256, 2)
+    assert ws > 2 * 3 * 2 * 256 * 128 * 2
+    assert L.sage_attention_host_workspace(1, 4, 256, 256, 0) == 0
+
+    def call(d=128, qb=64, causal=0, chunk=2, Nq=256, Nk=256, q=FAKE, wsb=ws, cs=FAKE, xs=FAKE + 64):
+        return L.sage_attention_host(q, FAKE, FAKE, FAKE, 1, 4, Nq, Nk, d, qb, 64, 0.0, causal, chunk, FAKE, wsb,
+                                     None, cs, xs)
+    assert call(d=64) == 2
+    assert call(qb=32) == 2
+    assert call(causal=2) == 1
+    assert call(causal=1, Nq=300) == 2     # causal needs Nq <= Nk
+    assert call(chunk=0) == 1
+    assert call(q=None) == 1
+    assert call(xs=FAKE) == 1               # the two streams must differ
+    assert call(xs=None) == 1
+    assert call(wsb=ws - 1) == 4

@@ -227,3 +227,31 @@ def test_dense_causal_full_size_videodit_sampled(cuda_lib):
         got = bf16_to_f64(out[0, h][torch.as_tensor(rows).cuda()])
         assert_output_close_rows(got, bits_to_f64(ref["out_bf16"]), f"videodit causal h{h}")
         check_lse(lse[0, h][torch.as_tensor(rows).cuda()], ref["lse"], f"videodit causal h{h}")
+
+
+@pytest.mark.parametrize("B,H,nq,nk,chunk,causal", [(2, 3, 300, 300, 4, False), (1, 5, 257, 513, 2, True),
+                                                    (1, 2, 129, 129, 8, False), (1, 7, 200, 333, 1, False)])
+def test_host_pipeline_equals_the_device_path(cuda_lib, B, H, nq, nk, chunk, causal):
+    """sage_attention_host (copies of one head group overlapped with the kernels of
+    the previous one) gives the same bits as the three device entry points; two
+    calls in a row share the workspace."""
+    w = synth.DenseWorkload(f"host_{B}_{H}_{nq}_{nk}", 13, B, H, nq, nk, 64, sub=(nq + nk) % 71)
+    x = synth.dense_inputs(w)
+
+    def host(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    hq, hk, hv = host(x["q"]), host(x["k"]), host(x["v"])
+    ref = cuda_lib.sage_attention(hq.cuda(), hk.cuda(), hv.cuda(), 64, 64, causal=causal)
+    side = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(cuda_lib.lib().sage_attention_host_workspace(B, H, nq, nk, chunk), dtype=torch.uint8,
+                     device="cuda")
+    with torch.cuda.stream(side):
+        for rep in range(2):
+            out = torch.full((B, H, nq, 128), float("nan"), dtype=torch.bfloat16).pin_memory()
+            cuda_lib.sage_attention_host(hq, hk, hv, out, 64, 64, causal=causal, head_chunk=chunk, workspace=ws,
+                                         status=status)
+            side.synchronize()
+            assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16)), f"call {rep}"
+    assert status.item() == 0
