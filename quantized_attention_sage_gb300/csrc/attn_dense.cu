@@ -44,7 +44,7 @@
 namespace sg {
 namespace dense {
 
-constexpr int BM = 128, BN = 128, NSK = 3, NSV = 2;
+constexpr int BM = 128, BN = 128, NSK = 2, NSV = 2;
 constexpr int kThreads = 384;
 constexpr uint32_t kQBytes = BM * kD * 2;    // 32 KB fp16 per query tile
 constexpr uint32_t kKBytes = BN * kD * 2;    // 32 KB fp16
