@@ -313,7 +313,7 @@ def run_ours(args, rank, world):
     # copies groups of heads in and out on a copy stream while the previous group runs
     hout = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(2, min(args.steps, 5))
-    head_chunk = 4
+    head_chunk = 6
     cstream, xstream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ws_host = torch.empty(L.sage_attention_host_workspace(B, H, N, N, head_chunk), dtype=torch.uint8, device=dev)
 

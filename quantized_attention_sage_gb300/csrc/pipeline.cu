@@ -2,7 +2,8 @@
 // with the host<->device copies overlapped with the kernels.
 //
 // The (batch, head) problems are independent, so the heads are cut into
-// chunks.  One copy stream moves chunk c+2's inputs in and chunk c's output
+// chunks (growing 1, 2, 4, ... up to the chunk size and shrinking again at
+// the end, so that the first copy in and the last copy out are short).  One copy stream moves chunk c+2's inputs in and chunk c's output
 // out while the compute stream quantizes and attends chunk c+1; inputs and
 // outputs are double-buffered in the caller's workspace, the intermediates
 // (codes, scales, fp16 images) are single-buffered because only the compute
@@ -106,7 +107,36 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), xs = static_cast<cudaStream_t>(copy_stream);
 
   const int BH = B * H;
-  const int C = sg::ceil_div(BH, L.hc);
+  // Chunk sizes: 1, 2, 4, ... up to head_chunk, head_chunk while heads
+  // remain, then halving again towards 1, so that the copies nothing can
+  // hide (the first chunk in, the last chunk out) are small.
+  std::vector<int> first;  // first head of each chunk, then BH
+  {
+    std::vector<int> up_sz, down_sz;
+    int left = BH;
+    for (int n = 1; n < L.hc && left > 0; n *= 2) {
+      const int a = n < left ? n : left;
+      up_sz.push_back(a);
+      left -= a;
+      if (left > 0) {
+        const int b = n < left ? n : left;
+        down_sz.push_back(b);
+        left -= b;
+      }
+    }
+    std::vector<int> mid;
+    while (left > 0) {
+      const int a = L.hc < left ? L.hc : left;
+      mid.push_back(a);
+      left -= a;
+    }
+    int h = 0;
+    for (int n : up_sz) first.push_back(h), h += n;
+    for (int n : mid) first.push_back(h), h += n;
+    for (auto it = down_sz.rbegin(); it != down_sz.rend(); ++it) first.push_back(h), h += *it;
+    first.push_back(h);
+  }
+  const int C = int(first.size()) - 1;
   std::vector<cudaEvent_t> in_ready(C, nullptr), done(C, nullptr);
   cudaEvent_t start = nullptr, last = nullptr;
   sage_status st = SAGE_OK;
@@ -128,10 +158,10 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
   if (st == SAGE_OK && ck(cudaEventRecord(start, cs))) ck(cudaStreamWaitEvent(xs, start, 0));
 
   const size_t qrow = size_t(Nq) * sg::kD * 2, krow = size_t(Nk) * sg::kD * 2;  // bytes per head
-  auto heads_of = [&](int c) { return (c + 1) * L.hc <= BH ? L.hc : BH - c * L.hc; };
+  auto heads_of = [&](int c) { return first[c + 1] - first[c]; };
   auto h2d = [&](int c) {
     const int s = c & 1, n = heads_of(c);
-    const size_t h0 = size_t(c) * L.hc;
+    const size_t h0 = size_t(first[c]);
     ck(cudaMemcpyAsync(ws + L.off_in[s][0], static_cast<const uint8_t *>(q_host) + h0 * qrow, n * qrow,
                        cudaMemcpyHostToDevice, xs));
     ck(cudaMemcpyAsync(ws + L.off_in[s][1], static_cast<const uint8_t *>(k_host) + h0 * krow, n * krow,
@@ -167,7 +197,7 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     }
     if (!ck(cudaEventRecord(done[c], cs))) break;
     if (!ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
-    ck(cudaMemcpyAsync(static_cast<uint8_t *>(out_host) + size_t(c) * L.hc * qrow, ws + L.off_out[s], n * qrow,
+    ck(cudaMemcpyAsync(static_cast<uint8_t *>(out_host) + size_t(first[c]) * qrow, ws + L.off_out[s], n * qrow,
                        cudaMemcpyDeviceToHost, xs));
     if (c + 2 < C) h2d(c + 2);
   }
