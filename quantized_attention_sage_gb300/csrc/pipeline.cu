@@ -3,8 +3,9 @@
 //
 // The (batch, head) problems are independent, so the heads are cut into
 // chunks (growing 1, 2, 4, ... up to the chunk size and shrinking again at
-// the end, so that the first copy in and the last copy out are short).  One copy stream moves chunk c+2's inputs in and chunk c's output
-// out while the compute stream quantizes and attends chunk c+1; inputs and
+// the end, so that the first copy in and the last copy out are short).  One
+// copy stream moves chunk c+2's inputs in and chunk c's output out while the
+// compute stream quantizes and attends chunk c+1; inputs and
 // outputs are double-buffered in the caller's workspace, the intermediates
 // (codes, scales, fp16 images) are single-buffered because only the compute
 // stream touches them.  Cross-stream order comes from events created for the
