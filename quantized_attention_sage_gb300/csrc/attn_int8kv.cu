@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
                                                           __nv_bfloat16 *__restrict__ kimg, __half *__restrict__ vtimg,
                                                           float *__restrict__ kt, float *__restrict__ vsf,
                                                           uint32_t *__restrict__ vmax_bits) {
-  __shared__ __half vt[kD][BN + 8];
+  __shared__ uint32_t vw[BN][kD / 4];  // the V tile's codes, key-major, 4 codes per word
   const int tile = blockIdx.x, g = blockIdx.y;
   const int key0 = tile * BN;
   const int8_t *ksrc = kc + g * kv_hs;
@@ -443,25 +443,45 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
-  // V: transpose through shared memory
+  // V: the int8 tile lands key-major in shared memory (16-byte loads and
+  // stores); each thread then reads one 4-code word of 8 consecutive keys
+  // (a warp reads 32 consecutive words of a key row: no bank conflicts),
+  // transposes the 4 x 8 bytes with byte permutes and writes 8 keys of each
+  // of its 4 channels as fp16.  An int8 code b becomes the fp16 bit pattern
+  // 0x6400 | (b ^ 0x80) = 1024 + b + 128, and subtracting 1152 leaves b.
 #pragma unroll
   for (int rep = 0; rep < 4; ++rep) {
-    const int e = threadIdx.x + 256 * rep;
-    const int key = e >> 3, c16 = (e & 7) * 16;
+    const int e = threadIdx.x + 256 * rep;  // 1024 chunks of 16 codes
+    const int key = e >> 3, w4 = (e & 7) * 4;
     const int gk = key0 + key;
     uint4 w = make_uint4(0, 0, 0, 0);
-    if (gk < Nk) w = *reinterpret_cast<const uint4 *>(vsrc + int64_t(gk) * kD + c16);
-    const int8_t *b = reinterpret_cast<const int8_t *>(&w);
-#pragma unroll
-    for (int u = 0; u < 16; ++u) vt[c16 + u][key] = __int2half_rn(b[u]);
+    if (gk < Nk) w = *reinterpret_cast<const uint4 *>(vsrc + int64_t(gk) * kD + 4 * w4);
+    *reinterpret_cast<uint4 *>(&vw[key][w4]) = w;
   }
   __syncthreads();
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
 #pragma unroll
-  for (int rep = 0; rep < 8; ++rep) {
-    const int e = threadIdx.x + 256 * rep;  // 2048 chunks of 8 keys
-    const int ch = e >> 4, k8 = (e & 15) * 8;
-    const uint4 val = *reinterpret_cast<const uint4 *>(&vt[ch][k8]);
-    *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + k8) = val;
+  for (int rep = 0; rep < 2; ++rep) {
+    const int e = threadIdx.x + 256 * rep;  // 512 tasks: word (4 channels) x group of 8 keys
+    const int wd = e & 31, kg = e >> 5;
+    uint32_t x[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = vw[kg * 8 + k][wd] ^ 0x80808080u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        // bytes c of keys k and k+1, each under a 0x64 high byte
+        const uint32_t t = __byte_perm(x[k], x[k + 1], uint32_t(c) | (uint32_t(4 + c) << 4));
+        const uint32_t hb = __byte_perm(t, 0x64646464u, 0x5140u);
+        const __half2 hv = __hsub2(*reinterpret_cast<const __half2 *>(&hb), bias);
+        o[k >> 1] = *reinterpret_cast<const uint32_t *>(&hv);
+      }
+      const int ch = 4 * wd + c;
+      *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + kg * 8) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
   }
   if (threadIdx.x < BN) {
     const int gk = key0 + threadIdx.x;
