@@ -255,3 +255,26 @@ def test_host_pipeline_equals_the_device_path(cuda_lib, B, H, nq, nk, chunk, cau
             side.synchronize()
             assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16)), f"call {rep}"
     assert status.item() == 0
+
+
+def test_dense_many_heads_and_batches(cuda_lib):
+    """B = 3, H = 101 (303 (b, h) problems in the grid's second dimension), ragged
+    length: a spread of heads against the oracle."""
+    w = synth.DenseWorkload("many_heads", 14, 3, 101, 70, 70, 64, sub=3)
+    x = synth.dense_inputs(w)
+    qk, vq, out = run_dense(cuda_lib, bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"]), 64, 64)
+    for b, h in ((0, 0), (0, 100), (1, 37), (2, 0), (2, 100)):
+        check_head(qk, vq, out, b, h, x["q"][b, h], x["k"][b, h], x["v"][b, h], 64, 64, tag=f"b{b}h{h}")
+
+
+def test_dense_causal_single_query_sees_every_key(cuda_lib):
+    """Nq = 1 causal over Nk keys: the one query is the last row, so it sees all keys
+    and equals the non-causal result bit for bit."""
+    w = synth.DenseWorkload("causal_one_query", 15, 1, 2, 1, 700, 64, sub=1)
+    x = synth.dense_inputs(w)
+    qk = cuda_lib.sage_quantize_qk(bf16_dev(x["q"]), bf16_dev(x["k"]), 64, 64)
+    vq = cuda_lib.sage_quantize_v(bf16_dev(x["v"]))
+    o1 = cuda_lib.sage_attn_fwd(qk, vq, 64, 64, causal=True)
+    o2 = cuda_lib.sage_attn_fwd(qk, vq, 64, 64)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))

@@ -43,6 +43,11 @@ SMALL = [
     synth.Int8KVWorkload("kv_g3_ragged", 9, 50, 129, 6, 2, sub=3),
     synth.Int8KVWorkload("kv_from_zero", 9, 200, 200, 4, 1, sub=4),
     synth.Int8KVWorkload("kv_one_query", 9, 1, 1000, 8, 8, sub=5),
+    # wide query-head groups: 5 (125 rows per tile), 32 (4 queries per tile) and
+    # the largest, 128 (one query per tile)
+    synth.Int8KVWorkload("kv_g5", 9, 37, 261, 10, 2, sub=8),
+    synth.Int8KVWorkload("kv_g32", 9, 9, 300, 64, 2, sub=9),
+    synth.Int8KVWorkload("kv_g128", 9, 3, 140, 128, 1, sub=10),
 ]
 
 
