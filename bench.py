@@ -65,6 +65,18 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model as lscpu reports it (empty if unavailable)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except (OSError, subprocess.TimeoutExpired):
+        return ""
+    for line in out.splitlines():
+        if line.strip().startswith("Model name:"):
+            return line.split(":", 1)[1].strip()
+    return ""
+
+
 def kernel_sha(name: str) -> str:
     p = os.path.join(ROOT, "quantized_attention_sage_gb300", "csrc", name)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()
@@ -307,6 +319,10 @@ def run_ours(args, rank, world):
         "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
         "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
     }
+    attn_ms = sorted(e[2].elapsed_time(e[3]) for e in evs)
+    comp["sage_attn_fwd_ms_p10_p50_p90"] = [attn_ms[int(0.1 * (len(attn_ms) - 1))],
+                                            attn_ms[int(0.5 * (len(attn_ms) - 1))],
+                                            attn_ms[int(0.9 * (len(attn_ms) - 1))]]
     value = whole_job_tflops(w.flops, world, ms_step)
 
     # ---- end to end through the public API with pinned host buffers: sage_attention_host
@@ -455,6 +471,7 @@ def run_ours(args, rank, world):
     if not args.no_cpu_baseline:
         cb = oracle_sample(args.cpu_seconds)
         line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        line["cpu_baseline"]["cpu"] = cpu_model()
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
