@@ -523,20 +523,9 @@ size_t dense_workspace_bytes(int B, int H, int Nq, int Nk) {
   return (size_t(B) * H * Nq + size_t(B) * H * Nk) * kD * sizeof(__half) + 256;
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 cudaError_t launch_codes_to_f16(const int8_t *codes, void *img, int64_t n, cudaStream_t st) {
   const int64_t n16 = n / 16;
-  const int64_t want = (n16 + 255) / 256, cap = int64_t(sm_count()) * 8;
+  const int64_t want = (n16 + 255) / 256, cap = int64_t(current_sm_count()) * 8;
   int blocks = int(want < cap ? want : cap);
   if (blocks < 1) blocks = 1;
   dense::codes_to_f16_kernel<<<blocks, 256, 0, st>>>(codes, static_cast<__half *>(img), n16);
@@ -585,12 +574,9 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.wait_ns = a.wait_ns;
   p.fault = a.fault;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(sage_attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static unsigned long long attr_done = 0;
+  e = set_smem_attr_once(reinterpret_cast<const void *>(sage_attn_fwd_kernel), kSmemBytes, &attr_done);
+  if (e != cudaSuccess) return e;
   dim3 grid(ceil_div(a.Nq, 2 * BM), BH);
   sage_attn_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();

@@ -546,17 +546,6 @@ struct Layout {
   size_t off_kimg, off_vt, off_kt, off_vs, off_vmax, off_po, off_pml, total;
 };
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
-
 static Layout layout(int Nq, int Hq, int Hkv, int Nk, int sms) {
   Layout L;
   L.G = Hq / Hkv;
@@ -598,12 +587,12 @@ static Layout layout(int Nq, int Hq, int Hkv, int Nk, int sms) {
 }  // namespace kv
 
 size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk) {
-  return kv::layout(Nq, Hq, Hkv, Nk, kv::sm_count()).total;
+  return kv::layout(Nq, Hq, Hkv, Nk, current_sm_count()).total;
 }
 
 cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   using namespace kv;
-  const Layout L = layout(a.Nq, a.Hq, a.Hkv, a.Nk, sm_count());
+  const Layout L = layout(a.Nq, a.Hq, a.Hkv, a.Nk, current_sm_count());
   uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255));
   auto *kimg = reinterpret_cast<__nv_bfloat16 *>(ws + L.off_kimg);
   auto *vtimg = reinterpret_cast<__half *>(ws + L.off_vt);
@@ -645,12 +634,9 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   p.part_o = po;
   p.part_ml = pml;
   p.status = a.status;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(int8kv_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static unsigned long long attr_done = 0;
+  e = set_smem_attr_once(reinterpret_cast<const void *>(int8kv_attn_kernel), kSmemBytes, &attr_done);
+  if (e != cudaSuccess) return e;
   int8kv_attn_kernel<<<dim3(L.nsplit, L.nqt, a.Hkv), kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -14,6 +14,14 @@ constexpr int kMeanChunk = 256;  // tokens per K-mean partial sum
 constexpr int kTile = 128;       // keys per softmax tile
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// SM count of the current device (queried per call: a process may drive GPUs
+// of different sizes).
+int current_sm_count();
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device):
+// the attribute belongs to the device's context, so a process-wide "done" flag
+// would leave a second device without it.
+cudaError_t set_smem_attr_once(const void *kernel, int bytes, unsigned long long *done_mask);
 __host__ __device__ inline int nk_pad(int nk) { return ceil_div(nk, kTile) * kTile; }
 
 // quantisers (quant.cu)
