@@ -278,3 +278,13 @@ def test_dense_causal_single_query_sees_every_key(cuda_lib):
     o2 = cuda_lib.sage_attn_fwd(qk, vq, 64, 64)
     torch.cuda.synchronize()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_dense_long_sequence_sampled(cuda_lib):
+    """One head of 200,003 tokens (1,563 key tiles per CTA, 782 CTAs): sampled rows
+    against the oracle, codes and scales in full."""
+    w = synth.DenseWorkload("long_seq", 16, 1, 1, 200003, 200003, 128, sub=1)
+    x = synth.dense_inputs(w)
+    qk, vq, out = run_dense(cuda_lib, bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"]), 128, 128)
+    rows = np.array([0, 1, 4095, 100000, 131071, 200002])
+    check_head(qk, vq, out, 0, 0, x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], 128, 128, rows=rows, tag="long")

@@ -96,3 +96,16 @@ def test_int8kv_full_size_sampled(cuda_lib, name):
     scale = np.abs(ref).max()
     print(f"{name}: max-abs {max_abs:.2e} rel-L2 {rel:.2e} (output scale {scale:.2f}); "
           f"vs unrounded fp64 max-abs {np.abs(got - ref).max():.2e}")
+
+
+def test_int8kv_quarter_million_token_cache_sampled(cuda_lib):
+    """64 queries at the end of a 262,144-token cache (2,048 key tiles, the largest
+    split-KV factor): sampled rows against the fp64 oracle."""
+    w = synth.Int8KVWorkload("kv_256k", 9, 64, 262144, 8, 2, sub=11)
+    x = synth.int8kv_inputs(w)
+    out = run(cuda_lib, w, x)
+    rows = np.array([0, 5, 31, 32, 63, 63, 17])
+    heads = np.array([0, 7, 3, 4, 0, 7, 5])
+    ref_b, _ = oracle_bf16(w, x, rows, heads)
+    got = bf16_to_f64(out[torch.as_tensor(rows).cuda(), torch.as_tensor(heads).cuda()])
+    assert_output_close(got, ref_b, w.name)
