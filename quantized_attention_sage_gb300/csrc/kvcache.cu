@@ -127,37 +127,55 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
   const void *src = isv ? a.v_src : a.k_src;
   int8_t *cache = isv ? a.v_cache : a.k_cache;
   __half *scale = static_cast<__half *>(isv ? a.v_scale : a.k_scale);
+  // raw source bytes of a row slice: 2 x 16 bytes (bf16) or 4 x 16 bytes (fp32)
+  constexpr int kVec = kF32 ? 4 : 2;
+  auto load = [&](int64_t pp, int tt, int hh, uint4 (&r)[kVec]) {
+    if (pp < P) {
+      const int64_t off = int64_t(tt) * a.src_tok + int64_t(hh) * a.src_head + 16 * l8;
+      const uint4 *s4 = kF32 ? reinterpret_cast<const uint4 *>(static_cast<const float *>(src) + off)
+                             : reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) r[u] = s4[u];
+    } else {
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) r[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  uint4 nxt[kVec];
+  load(p, t, h, nxt);
   for (; q < qend; ++q) {
+    // this couple's bytes; the next couple's loads are issued before the math
+    uint4 cur[kVec];
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) cur[u] = nxt[u];
     const bool live = p < P;
+    const int tc = t, hcur = h;
+    p += 2;
+    h += 2;
+    while (h >= a.Hkv) {
+      h -= a.Hkv;
+      ++t;
+    }
+    if (q + 1 < qend) load(p, t, h, nxt);
     float x[16];
-    if (live) {
-      const int64_t off = int64_t(t) * a.src_tok + int64_t(h) * a.src_head + 16 * l8;
-      if (kF32) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + off);
+    if (kF32) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 v = s4[u];
-          x[4 * u] = v.x;
-          x[4 * u + 1] = v.y;
-          x[4 * u + 2] = v.z;
-          x[4 * u + 3] = v.w;
-        }
-      } else {
-        const uint4 *s4 = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 w = s4[u];
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            x[8 * u + 2 * k] = __uint_as_float(ww[k] << 16);
-            x[8 * u + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
-          }
-        }
+      for (int u = 0; u < kVec; ++u) {
+        x[4 * u] = __uint_as_float(cur[u].x);
+        x[4 * u + 1] = __uint_as_float(cur[u].y);
+        x[4 * u + 2] = __uint_as_float(cur[u].z);
+        x[4 * u + 3] = __uint_as_float(cur[u].w);
       }
     } else {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) x[k] = 0.f;
+      for (int u = 0; u < kVec; ++u) {
+        const uint32_t ww[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          x[8 * u + 2 * k] = __uint_as_float(ww[k] << 16);
+          x[8 * u + 2 * k + 1] = __uint_as_float(ww[k] & 0xFFFF0000u);
+        }
+      }
     }
     float amax = 0.f;
 #pragma unroll
@@ -170,30 +188,28 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
     if (sc > 0.f) {
       const float inv = __frcp_rn(sc);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float qq = __fmul_rn(x[k], inv);
-        float rq = rintf(qq);
-        if (0.5f - fabsf(qq - rq) < 1e-4f) rq = rintf(__fdiv_rn(x[k], sc));
-        int c = int(rq);
-        c = c > 127 ? 127 : (c < -127 ? -127 : c);
-        packed[k >> 2] |= (uint32_t(c) & 0xFFu) << (8 * (k & 3));
+      for (int k4 = 0; k4 < 4; ++k4) {
+        int c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float xv = x[4 * k4 + u];
+          const float qq = __fmul_rn(xv, inv);
+          int cv = __float2int_rn(qq);  // round half to even, as rint
+          if (fabsf(__fsub_rn(qq, float(cv))) > 0.5f - 1e-4f) cv = __float2int_rn(__fdiv_rn(xv, sc));
+          c[u] = max(-127, min(127, cv));
+        }
+        // bytes 0 of c0..c3 -> one word
+        packed[k4] = __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
       }
     }
     if (live) {
-      const int64_t pos = int64_t(a.pos0) + t;
-      *reinterpret_cast<uint4 *>(cache + int64_t(h) * a.cache_head + pos * kD + 16 * l8) =
+      const int64_t pos = int64_t(a.pos0) + tc;
+      *reinterpret_cast<uint4 *>(cache + int64_t(hcur) * a.cache_head + pos * kD + 16 * l8) =
           make_uint4(packed[0], packed[1], packed[2], packed[3]);
       if (l8 == 0) {
-        scale[int64_t(h) * a.scale_head + pos] = s16;
+        scale[int64_t(hcur) * a.scale_head + pos] = s16;
         if (!(fabsf(sc) <= 65504.f) && a.status) atomicCAS(a.status, 0, SAGE_ERR_NONFINITE);
       }
-    }
-    // next couple: pair p + 2
-    p += 2;
-    h += 2;
-    while (h >= a.Hkv) {
-      h -= a.Hkv;
-      ++t;
     }
   }
 }
