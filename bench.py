@@ -485,12 +485,27 @@ def run_case(args):
 
     qas.build()
     torch.cuda.set_device(0)
+    before = None
     if args.case == "dense":
         w = synth.DenseWorkload("profile_case", 11, 1, args.heads, args.seq, args.seq, 128)
         x = synth.dense_inputs(w)
         q, k, v = (torch.from_numpy(x[t].view(np.int16)).view(torch.bfloat16).cuda() for t in ("q", "k", "v"))
         run = lambda: qas.sage_attention(q, k, v, 128, 128)  # noqa: E731
         flops = w.flops
+    elif args.case == "kvcache":
+        # int8 KV-cache writer: args.seq tokens x args.heads kv heads of bf16 K and V rows
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(5)
+        kr = torch.randn((args.seq, args.heads, 128), generator=gen, device="cuda").to(torch.bfloat16)
+        vr = torch.randn((args.seq, args.heads, 128), generator=gen, device="cuda").to(torch.bfloat16)
+        kc = torch.empty((args.heads, args.seq, 128), dtype=torch.int8, device="cuda")
+        vc = torch.empty_like(kc)
+        ks = torch.empty((args.heads, args.seq), dtype=torch.float16, device="cuda")
+        vs = torch.empty_like(ks)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        before = flush.zero_  # cold L2 for the writer, outside the timed call
+        run = lambda: qas.int8kv_cache_write(kr, vr, kc, ks, vc, vs, 0)  # noqa: E731
+        flops = 0
     else:
         wk = synth.Int8KVWorkload("profile_case", 12, args.queries, args.seq, args.heads, max(1, args.heads // 4))
         y = synth.int8kv_inputs(wk)
@@ -500,16 +515,23 @@ def run_case(args):
         run = lambda: qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0)  # noqa: E731
         flops = wk.flops
     for _ in range(args.reps):
+        if before is not None:
+            before()
         run()
     torch.cuda.synchronize()
+    if before is not None:
+        before()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     run()
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    print(json.dumps({"case": args.case, "heads": args.heads, "seq": args.seq, "ms": ms,
-                      "tflops": flops / (ms * 1e-3) / 1e12}))
+    res = {"case": args.case, "heads": args.heads, "seq": args.seq, "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    if args.case == "kvcache":
+        nbytes = args.seq * args.heads * (2 * 256 + 2 * 128 + 2 * 2)
+        res.update(bytes=nbytes, gbs=nbytes / (ms * 1e-3) / 1e9)
+    print(json.dumps(res))
 
 
 def main():
@@ -520,7 +542,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--case", choices=["dense", "int8kv"], default=None,
+    ap.add_argument("--case", choices=["dense", "int8kv", "kvcache"], default=None,
                     help="run a small workload of one path (profiler captures) instead of the bench")
     ap.add_argument("--heads", type=int, default=24)
     ap.add_argument("--seq", type=int, default=8192)
