@@ -34,12 +34,15 @@ __global__ void __launch_bounds__(64) chunk_reduce_kernel(const __nv_bfloat16 *_
   const int t1 = min(t0 + kMeanChunk, N);
   float a0 = 0.f, a1 = 0.f;
   int t = t0;
-  for (; t + 8 <= t1; t += 8) {
-    __nv_bfloat162 v[8];
+  // 32 rows of loads in flight per round (the additions stay in ascending
+  // token order): with few heads each chunk's CTA is alone on its SM and the
+  // chunk time is the number of memory round trips
+  for (; t + 32 <= t1; t += 32) {
+    __nv_bfloat162 v[32];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const __nv_bfloat162 *>(base + int64_t(t + u) * sn);
+    for (int u = 0; u < 32; ++u) v[u] = *reinterpret_cast<const __nv_bfloat162 *>(base + int64_t(t + u) * sn);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < 32; ++u) {
       const float2 f = __bfloat1622float2(v[u]);
       if (kMax) {
         a0 = fmaxf(a0, fabsf(f.x));
@@ -69,7 +72,16 @@ __global__ void __launch_bounds__(128) k_mean_finalize_kernel(const float *__res
   const int bh = blockIdx.x, c = threadIdx.x;
   const float *p = partial + int64_t(bh) * nchunks * kD + c;
   float tot = 0.f;
-  for (int i = 0; i < nchunks; ++i) tot = __fadd_rn(tot, p[int64_t(i) * kD]);
+  int i = 0;
+  // 16 partials loaded per round, added in ascending chunk order
+  for (; i + 16 <= nchunks; i += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = p[int64_t(i + u) * kD];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) tot = __fadd_rn(tot, v[u]);
+  }
+  for (; i < nchunks; ++i) tot = __fadd_rn(tot, p[int64_t(i) * kD]);
   mean[bh * kD + c] = __fdiv_rn(tot, float(Nk));
 }
 
@@ -171,7 +183,15 @@ __global__ void __launch_bounds__(128) v_finalize_kernel(const float *__restrict
   const int bh = blockIdx.x, c = threadIdx.x;
   const float *p = partial + int64_t(bh) * nchunks * kD + c;
   float amax = 0.f;
-  for (int i = 0; i < nchunks; ++i) amax = fmaxf(amax, p[int64_t(i) * kD]);
+  int i = 0;
+  for (; i + 16 <= nchunks; i += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) v[u] = p[int64_t(i + u) * kD];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) amax = fmaxf(amax, v[u]);
+  }
+  for (; i < nchunks; ++i) amax = fmaxf(amax, p[int64_t(i) * kD]);
   v_scales[bh * kD + c] = __fdiv_rn(amax, 448.f);
   inv[bh * kD + c] = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
 }
