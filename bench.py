@@ -77,6 +77,12 @@ def cpu_model() -> str:
     return ""
 
 
+def current_sms(dev) -> int:
+    import torch
+
+    return torch.cuda.get_device_properties(dev).multi_processor_count
+
+
 def kernel_sha(name: str) -> str:
     p = os.path.join(ROOT, "quantized_attention_sage_gb300", "csrc", name)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()
@@ -460,7 +466,10 @@ def run_ours(args, rank, world):
                      "bound": "tensor", "achieved": achieved, "peak": peak_mixed, "unit": "TFLOP/s",
                      "frac": achieved / peak_mixed, "traffic": traffic,
                      "peak_note": (f"{pk['source']}: bf16 burst {p16} TFLOP/s for the Q.K^T half, x2 (nominal "
-                                   f"fp8/bf16 ratio) for the P.V half")},
+                                   f"fp8/bf16 ratio) for the P.V half"),
+                     # the softmax's MUFU demand: one ex2 per score
+                     "exp2_per_sm_per_clock": (w.B * w.H * w.Nq * w.Nk) / (comp["sage_attn_fwd_ms"] * 1e-3)
+                     / (current_sms(dev) * 1e6 * ((clocks or {}).get("sm_mhz") or 2070.0))},
         "components": comp,
         "causal_lse": causal,
         "int8kv": kv,
