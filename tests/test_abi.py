@@ -149,3 +149,16 @@ def test_host_pipeline_rejects_bad_arguments(L):
     assert call(xs=FAKE) == 1               # the two streams must differ
     assert call(xs=None) == 1
     assert call(wsb=ws - 1) == 4
+
+
+def test_attn_fwd_ex_rejects_bad_arguments(L):
+    st = s4(2 * 256 * 128, 256 * 128, 128)
+
+    def call(causal=0, Nq=256, Nk=256, lse=None):
+        return L.sage_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, Nq, Nk, 128, 64, 64, 0.0, causal, FAKE,
+                                  st, lse, FAKE, 1 << 30, None, None)
+    assert call(causal=2) == 1                 # causal is 0 or 1
+    assert call(causal=1, Nq=300) == 2         # the causal window needs Nq <= Nk
+    assert call(lse=FAKE + 2) == 1             # lse must be 4-byte aligned
+    assert L.sage_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 96, 64, 64, 0.0, 0, FAKE, st,
+                              None, FAKE, 1 << 30, None, None) == 2   # d != 128
