@@ -350,15 +350,19 @@ def run_ours(args, rank, world):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
     e0.record(cstream)
-    for _ in range(e2e_steps):
+    step_ev[0].record(cstream)
+    for i in range(e2e_steps):
         e2e_step()
+        step_ev[i + 1].record(cstream)
     e1.record(cstream)
     torch.cuda.synchronize()
     assert status.item() == 0, "device status set during the e2e steps"
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(e2e_steps)]
     e2e = {"value": whole_job_tflops(w.flops, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
-           "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
+           "ms_each_step": per_step, "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
            "api": f"sage_attention_host, head_chunk={head_chunk}, pinned host buffers"}
     del ws_host
 
