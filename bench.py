@@ -444,6 +444,17 @@ def run_ours(args, rank, world):
 
     pk = peaks()
     kv["cache_write_32k_bf16"]["frac_hbm"] = kv["cache_write_32k_bf16"]["gbs"] / pk["hbm_gbs"]
+    # the quantisers against the measured copy bandwidth: algorithmic bytes are
+    # Q and K read (bf16) + codes written for sage_quantize_qk, V read + codes
+    # written (padded to 128 tokens) for sage_quantize_v
+    elems = w.B * w.H * w.Nk * 128
+    qbytes = {"sage_quantize_qk": 2 * elems * 2 + 2 * elems,
+              "sage_quantize_v": elems * 2 + w.B * w.H * 128 * qas.nk_pad(w.Nk)}
+    quantizers = {}
+    for name, nb in qbytes.items():
+        ms_q = comp[name + "_ms"]
+        quantizers[name] = {"ms": ms_q, "bytes": nb, "gbs": nb / (ms_q * 1e-3) / 1e9,
+                            "frac_hbm": nb / (ms_q * 1e-3) / 1e9 / pk["hbm_gbs"]}
     p16 = pk["bf16_tflops"]
     for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
         # Q.K^T and P.V both on the bf16/f16 tensor path; the fp16 hi/lo split of
@@ -475,6 +486,7 @@ def run_ours(args, rank, world):
                      "exp2_per_sm_per_clock": (w.B * w.H * w.Nq * w.Nk) / (comp["sage_attn_fwd_ms"] * 1e-3)
                      / (current_sms(dev) * 1e6 * ((clocks or {}).get("sm_mhz") or 2070.0))},
         "components": comp,
+        "quantizers": quantizers,
         "causal_lse": causal,
         "int8kv": kv,
         "clocks": clocks,
