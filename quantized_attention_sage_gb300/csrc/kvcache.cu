@@ -20,7 +20,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sg {
 namespace kvc {
@@ -185,21 +188,36 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
     const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
     const float sc = __half2float(s16);
     uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    // With a normal fp16 scale (>= 2^-14), |x / s| <= 127 (1 + 2^-11), so the
+    // codes need no clamp; only fp16-subnormal scales can exceed 127.  (The
+    // vote is taken by the whole warp, before any lane branches.)
+    const bool clamp = __any_sync(0xffffffffu, sc > 0.f && sc < 6.103515625e-05f);
     if (sc > 0.f) {
       const float inv = __frcp_rn(sc);
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
+      auto encode4 = [&](int k4, auto clamp_c) {
         int c[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float xv = x[4 * k4 + u];
-          const float qq = __fmul_rn(xv, inv);
-          int cv = __float2int_rn(qq);  // round half to even, as rint
-          if (fabsf(__fsub_rn(qq, float(cv))) > 0.5f - 1e-4f) cv = __float2int_rn(__fdiv_rn(xv, sc));
-          c[u] = max(-127, min(127, cv));
+        for (int u = 0; u < 4; u += 2) {
+          const float2 q2 = fmul2(make_float2(x[4 * k4 + u], x[4 * k4 + u + 1]), make_float2(inv, inv));
+          const float qv[2] = {q2.x, q2.y};
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            int cv = __float2int_rn(qv[v]);  // round half to even, as rint
+            if (fabsf(__fsub_rn(qv[v], float(cv))) > 0.5f - 1e-4f)
+              cv = __float2int_rn(__fdiv_rn(x[4 * k4 + u + v], sc));
+            if (decltype(clamp_c)::value) cv = max(-127, min(127, cv));
+            c[u + v] = cv;
+          }
         }
         // bytes 0 of c0..c3 -> one word
-        packed[k4] = __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
+        return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
+      };
+      if (clamp) {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) packed[k4] = encode4(k4, std::true_type{});
+      } else {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) packed[k4] = encode4(k4, std::false_type{});
       }
     }
     if (live) {
