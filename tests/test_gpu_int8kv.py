@@ -109,3 +109,22 @@ def test_int8kv_quarter_million_token_cache_sampled(cuda_lib):
     ref_b, _ = oracle_bf16(w, x, rows, heads)
     got = bf16_to_f64(out[torch.as_tensor(rows).cuda(), torch.as_tensor(heads).cuda()])
     assert_output_close(got, ref_b, w.name)
+
+
+def test_int8kv_strided_queries_and_output(cuda_lib):
+    """q read through a [Nq, Hq, 192] buffer's first 128 channels and the output
+    written into a [Nq, Hq + 3, 128] buffer give the same bits as contiguous ones."""
+    w = synth.Int8KVWorkload("kv_strided", 9, 45, 400, 8, 2, sub=12)
+    x = synth.int8kv_inputs(w)
+    q, kc, ks, vc, vs = to_dev(x)
+    ref = cuda_lib.int8kv_prompt_attn(q, kc, ks, vc, vs, w.q_pos0)
+    wide = torch.zeros((w.Nq, w.Hq, 192), dtype=torch.bfloat16, device="cuda")
+    wide[:, :, :128] = q
+    qv = wide[:, :, :128]
+    big = torch.full((w.Nq, w.Hq + 3, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ov = big[:, 1:w.Hq + 1, :]
+    assert not qv.is_contiguous() and not ov.is_contiguous()
+    cuda_lib.int8kv_prompt_attn(qv, kc, ks, vc, vs, w.q_pos0, out=ov)
+    torch.cuda.synchronize()
+    assert torch.equal(ov.view(torch.int16), ref.view(torch.int16))
+    assert torch.isnan(big[:, 0].float()).all() and torch.isnan(big[:, w.Hq + 1:].float()).all()
