@@ -128,6 +128,26 @@ def _strides4(t) -> Strides:
     return Strides(t.stride(0), t.stride(1), t.stride(2))
 
 
+def _require(t, dtype, name: str, dims: int = None):
+    """Device tensors only: there is no CPU path."""
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimensions, got {t.dim()}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+
+
+def _require_codes(torch, qk: dict, vq: dict):
+    """The attention calls take the quantisers' outputs as they come."""
+    _require(qk["q_codes"], torch.int8, "q_codes", 4)
+    _require(qk["k_codes"], torch.int8, "k_codes", 4)
+    _require(qk["q_scales"], torch.float32, "q_scales")
+    _require(qk["k_scales"], torch.float32, "k_scales")
+    _require(vq["v_codes"], torch.uint8, "v_codes", 4)
+    _require(vq["v_scales"], torch.float32, "v_scales")
+
+
 def _check(code: int, where: str):
     if code != 0:
         raise SageError(code, where)
@@ -152,6 +172,10 @@ def sage_quantize_qk(q, k, q_block: int = 64, k_block: int = 64, out=None, works
     q: [B,H,Nq,128] bf16, k: [B,H,Nk,128] bf16 (any 16-byte aligned strides).
     Returns dict(q_codes, q_scales, k_codes, k_scales, k_mean)."""
     torch = _torch()
+    _require(q, torch.bfloat16, "q", 4)
+    _require(k, torch.bfloat16, "k", 4)
+    if q.shape[:2] != k.shape[:2] or q.shape[3] != D or k.shape[3] != D or q.device != k.device:
+        raise ValueError("q and k must be [B, H, N, 128] on one device with the same B and H")
     B, H, Nq, _ = q.shape
     Nk = k.shape[2]
     dev = q.device
@@ -179,6 +203,9 @@ def nk_pad(nk: int) -> int:
 def sage_quantize_v(v, out=None, workspace=None, stream=None):
     """FP8 E4M3 per-channel codes of V, transposed to [B,H,128,Nk_pad], and scales [B,H,128]."""
     torch = _torch()
+    _require(v, torch.bfloat16, "v", 4)
+    if v.shape[3] != D:
+        raise ValueError("v must be [B, H, Nk, 128]")
     B, H, Nk, _ = v.shape
     dev = v.device
     if out is None:
@@ -200,6 +227,7 @@ def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_s
     ``causal``: query i sees keys j <= i + (Nk - Nq).  ``return_lse``: also return the
     rows' natural log-sum-exp, fp32 [B,H,Nq]."""
     torch = _torch()
+    _require_codes(torch, qk, vq)
     qc, kc = qk["q_codes"], qk["k_codes"]
     B, H, Nq, _ = qc.shape
     Nk = kc.shape[2]
@@ -229,6 +257,7 @@ def sage_attn_fwd_scores_dump(qk: dict, vq: dict, q_block: int = 64, k_block: in
 
     Returns (out bf16 [B,H,Nq,128], scores int32 [B,H,Nq_pad,Nk_pad]).  For checking small problems."""
     torch = _torch()
+    _require_codes(torch, qk, vq)
     qc, kc = qk["q_codes"], qk["k_codes"]
     B, H, Nq, _ = qc.shape
     Nk = kc.shape[2]
@@ -253,6 +282,7 @@ def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: in
     Returns the device status word after synchronising (SAGE_ERR_TIMEOUT when the
     failure detection works).  Test hook: the output is not written."""
     torch = _torch()
+    _require_codes(torch, qk, vq)
     qc, kc = qk["q_codes"], qk["k_codes"]
     B, H, Nq, _ = qc.shape
     Nk = kc.shape[2]

@@ -162,3 +162,26 @@ def test_attn_fwd_ex_rejects_bad_arguments(L):
     assert call(lse=FAKE + 2) == 1             # lse must be 4-byte aligned
     assert L.sage_attn_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 96, 64, 64, 0.0, 0, FAKE, st,
                               None, FAKE, 1 << 30, None, None) == 2   # d != 128
+
+
+def test_binding_rejects_wrong_dtypes_and_host_tensors():
+    """The Python binding checks dtypes, ranks and the device before it calls the
+    library, so a CPU tensor is an error, never a silent host computation."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        qas.sage_quantize_qk(q, q)
+    with pytest.raises(ValueError, match="bfloat16"):
+        qas.sage_quantize_qk(q.float(), q)
+    with pytest.raises(ValueError, match="CUDA"):
+        qas.sage_quantize_v(q)
+    with pytest.raises(ValueError, match="dimensions"):
+        qas.sage_quantize_v(q[0])
+    qk = dict(q_codes=torch.zeros((1, 1, 64, 128), dtype=torch.int8),
+              k_codes=torch.zeros((1, 1, 64, 128), dtype=torch.int8),
+              q_scales=torch.zeros((1, 1, 1)), k_scales=torch.zeros((1, 1, 1)))
+    vq = dict(v_codes=torch.zeros((1, 1, 128, 128), dtype=torch.uint8), v_scales=torch.zeros((1, 1, 128)))
+    with pytest.raises(ValueError, match="CUDA"):
+        qas.sage_attn_fwd(qk, vq)
+    with pytest.raises(ValueError, match="int8"):
+        qas.sage_attn_fwd(dict(qk, q_codes=qk["q_codes"].to(torch.uint8)), vq)
