@@ -196,21 +196,25 @@ sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const
 
 /* ------------------------------------------------------------------------
  * sage_attention_host - the dense path (sage_quantize_qk, sage_quantize_v,
- * sage_attn_fwd_ex) on HOST buffers, with the host<->device copies of one
- * group of heads overlapped with the kernels of the previous group.  The
- * (batch, head) problems are independent ("H3 Performance Roadmap", section
- * "Phase 4: Dense Sage-Compatible Attention": one dense attention per head),
- * so the B*H heads are cut into chunks of head_chunk; one copy stream moves
- * chunk c+2 in and chunk c out while the compute stream runs chunk c+1.
+ * sage_attn_fwd_ex) on HOST buffers, with the host<->device copies and the
+ * quantizers of one group of heads overlapped with the attention of another.
+ * The (batch, head) problems are independent ("H3 Performance Roadmap",
+ * section "Phase 4: Dense Sage-Compatible Attention": one dense attention per
+ * head), so the B*H heads are cut into chunks of up to head_chunk heads
+ * (1, 2, 4, ... at the start and the end); the copy stream moves chunk c+2
+ * in, chunk c out and quantizes chunk c+2 while the compute stream runs the
+ * attention of chunk c+1.
  *   q_host, out_host: bf16 [B][H][Nq][128] contiguous; k_host, v_host: bf16
  *     [B][H][Nk][128] contiguous.  Page-locked memory lets the copies overlap
  *     the kernels (pageable memory works, without overlap).
  *   head_chunk >= 1: heads per chunk (the last chunk may be smaller).
  *   causal: 0 or 1 as in sage_attn_fwd_ex (no lse here).
  *   workspace: device memory of sage_attention_host_workspace(B, H, Nq, Nk,
- *     head_chunk) bytes (double-buffered bf16 chunks, codes, scales and the
- *     three entry points' workspaces); shared by successive calls.
- *   compute_stream, copy_stream: two different streams.  Everything is
+ *     head_chunk) bytes (double-buffered bf16 chunks, codes, scales and
+ *     quantizer workspaces, one attention workspace); shared by successive
+ *     calls.
+ *   compute_stream, copy_stream: two different streams (the copy stream
+ *     also runs the quantizer kernels).  Everything is
  *     enqueued asynchronously; out_host is complete once compute_stream has
  *     reached the end of the call (it waits for the last copy).  The copies
  *     start after the work already queued on compute_stream.

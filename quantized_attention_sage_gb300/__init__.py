@@ -316,9 +316,10 @@ def sage_attention_host(q, k, v, out, q_block: int = 64, k_block: int = 64, sm_s
                         causal: bool = False, head_chunk: int = 4, workspace=None, status=None, stream=None,
                         copy_stream=None):
     """The dense path on host tensors q, out [B,H,Nq,128] and k, v [B,H,Nk,128] (bf16, contiguous;
-    page-locked for the copies to overlap the kernels).  Groups of ``head_chunk`` heads are copied
-    in on ``copy_stream`` while the previous group is computed on ``stream``; ``out`` is complete once
-    ``stream`` reaches the end of the call.  Both streams must differ (non-default streams overlap)."""
+    page-locked for the copies to overlap the kernels).  Groups of up to ``head_chunk`` heads are
+    copied in and out and quantized on ``copy_stream`` while the attention of another group runs on
+    ``stream``; ``out`` is complete once ``stream`` reaches the end of the call.  Both streams must
+    differ (non-default streams overlap)."""
     torch = _torch()
     for t in (q, k, v, out):
         if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:

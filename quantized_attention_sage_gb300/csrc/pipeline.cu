@@ -1,26 +1,34 @@
 // sage_attention_host: the dense path on host-resident Q, K, V and output,
-// with the host<->device copies overlapped with the kernels.
+// with the host<->device copies and the quantizers overlapped with the
+// attention kernels.
 //
 // The (batch, head) problems are independent, so the heads are cut into
 // chunks (growing 1, 2, 4, ... up to the chunk size and shrinking again at
-// the end, so that the first copy in and the last copy out are short).  One
-// copy stream moves chunk c+2's inputs in and chunk c's output out while the
-// compute stream quantizes and attends chunk c+1; inputs and
-// outputs are double-buffered in the caller's workspace, the intermediates
-// (codes, scales, fp16 images) are single-buffered because only the compute
-// stream touches them.  Cross-stream order comes from events created for the
-// call (timing disabled) and released as soon as they are enqueued.
+// the end, so that the first copy in and the last copy out are short).  Two
+// streams share the work:
+//   staging stream (the caller's copy stream): host->device copies, the two
+//            quantizers, device->host copies;
+//   compute stream: the attention of one chunk after another.
+// While the compute stream attends chunk c, the staging stream copies chunk
+// c+2 in, then (once chunk c is done) copies its output out and quantizes
+// chunk c+2, so that neither the copies nor the short quantizer launches
+// sit between two attention launches.  Inputs, outputs and the quantized
+// intermediates are double-buffered in the caller's workspace (slot c % 2);
+// the attention workspace is single-buffered because only the compute stream
+// touches it.  Cross-stream order comes from events created for the call
+// (timing disabled) and released as soon as they are enqueued.
 //
-// Per chunk c (slot s = c % 2):
-//   copy:    H2D q, k, v -> in[s]          record in_ready[c]
-//   compute: wait in_ready[c]; quantize Q/K, quantize V, attention
-//            -> out[s]                     record done[c]
-//   copy:    wait done[c]; D2H out[s]; then H2D of chunk c+2 into in[s]
-// H2D(c+2) follows done[c] (in[s] has been read) and D2H(c) on the copy
-// stream, so compute(c+2), which waits for in_ready[c+2], also finds out[s]
-// drained.  The copy stream first waits for the work already queued on the
-// compute stream; at the end the compute stream waits for the last D2H, so
-// the caller synchronises one stream.
+// Per chunk c (slot s = c % 2), in stream order:
+//   staging: H2D q, k, v -> in[s]; quantize in[s] -> codes[s]; record q_ready[c]
+//   compute: wait q_ready[c]; attention codes[s] -> out[s]; record done[c]
+//   staging: wait done[c]; D2H out[s]; quantize chunk c+2 into codes[s]
+// H2D of chunk c+2 is queued before the wait for done[c]: in[s] was last read
+// by the quantizers of chunk c, earlier on the same stream.  The quantizers
+// of chunk c+2 follow done[c] (codes[s] has been read) and D2H of chunk c
+// (out[s] is drained before attention(c+2), which waits for q_ready[c+2]).
+// The staging stream first waits for the work already queued on the compute
+// stream; at the end the compute stream waits for the last D2H, so the caller
+// synchronises one stream.
 #include <cuda_runtime.h>
 
 #include <vector>
@@ -34,10 +42,11 @@ constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 struct HostLayout {
-  int hc;                                  // heads per chunk
-  size_t q_bytes, k_bytes, o_bytes;        // bf16 chunk buffers
-  size_t off_in[2][3], off_out[2];         // double-buffered inputs (q, k, v) and output
-  size_t off_qc, off_kc, off_qs, off_ks, off_mu, off_vc, off_vs, off_wqk, off_wv, off_wa;
+  int hc;                               // heads per chunk
+  size_t q_bytes, k_bytes, o_bytes;     // bf16 chunk buffers
+  size_t off_in[2][3], off_out[2];      // inputs (q, k, v) and output per slot
+  size_t off_qc[2], off_kc[2], off_qs[2], off_ks[2], off_mu[2], off_vc[2], off_vs[2], off_wqk[2], off_wv[2];
+  size_t off_wa;                        // attention workspace (compute stream only)
   size_t wqk, wv, wa, total;
 };
 
@@ -49,6 +58,9 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
   L.q_bytes = hc * Nq * sg::kD * 2;
   L.k_bytes = hc * Nk * sg::kD * 2;
   L.o_bytes = L.q_bytes;
+  L.wqk = sage_quantize_qk_workspace(1, L.hc, Nk);
+  L.wv = sage_quantize_v_workspace(1, L.hc, Nk);
+  L.wa = sage_attn_fwd_workspace(1, L.hc, Nq, Nk);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -60,22 +72,48 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
     L.off_in[s][1] = take(L.k_bytes);
     L.off_in[s][2] = take(L.k_bytes);
     L.off_out[s] = take(L.o_bytes);
+    L.off_qc[s] = take(hc * Nq * sg::kD);
+    L.off_kc[s] = take(hc * Nk * sg::kD);
+    L.off_qs[s] = take(hc * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
+    L.off_ks[s] = take(hc * sg::ceil_div(Nk, 64) * sizeof(float));
+    L.off_mu[s] = take(hc * sg::kD * sizeof(float));
+    L.off_vc[s] = take(hc * sg::kD * size_t(sg::nk_pad(Nk)));
+    L.off_vs[s] = take(hc * sg::kD * sizeof(float));
+    L.off_wqk[s] = take(L.wqk);
+    L.off_wv[s] = take(L.wv);
   }
-  L.off_qc = take(hc * Nq * sg::kD);
-  L.off_kc = take(hc * Nk * sg::kD);
-  L.off_qs = take(hc * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
-  L.off_ks = take(hc * sg::ceil_div(Nk, 64) * sizeof(float));
-  L.off_mu = take(hc * sg::kD * sizeof(float));
-  L.off_vc = take(hc * sg::kD * size_t(sg::nk_pad(Nk)));
-  L.off_vs = take(hc * sg::kD * sizeof(float));
-  L.wqk = sage_quantize_qk_workspace(1, L.hc, Nk);
-  L.wv = sage_quantize_v_workspace(1, L.hc, Nk);
-  L.wa = sage_attn_fwd_workspace(1, L.hc, Nq, Nk);
-  L.off_wqk = take(L.wqk);
-  L.off_wv = take(L.wv);
   L.off_wa = take(L.wa);
   L.total = off + kAlign;  // room to align the base
   return L;
+}
+
+// First head of each chunk, then B*H: sizes 1, 2, 4, ... up to hc, hc while
+// heads remain, then halving again towards 1, so that the copies nothing can
+// hide (the first chunk in, the last chunk out) are small.
+std::vector<int> chunk_starts(int BH, int hc) {
+  std::vector<int> up_sz, down_sz, mid, first;
+  int left = BH;
+  for (int n = 1; n < hc && left > 0; n *= 2) {
+    const int a = n < left ? n : left;
+    up_sz.push_back(a);
+    left -= a;
+    if (left > 0) {
+      const int b = n < left ? n : left;
+      down_sz.push_back(b);
+      left -= b;
+    }
+  }
+  while (left > 0) {
+    const int a = hc < left ? hc : left;
+    mid.push_back(a);
+    left -= a;
+  }
+  int h = 0;
+  for (int n : up_sz) first.push_back(h), h += n;
+  for (int n : mid) first.push_back(h), h += n;
+  for (auto it = down_sz.rbegin(); it != down_sz.rend(); ++it) first.push_back(h), h += *it;
+  first.push_back(h);
+  return first;
 }
 
 }  // namespace
@@ -107,38 +145,9 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
                                             ~uintptr_t(kAlign - 1));
   cudaStream_t cs = static_cast<cudaStream_t>(compute_stream), xs = static_cast<cudaStream_t>(copy_stream);
 
-  const int BH = B * H;
-  // Chunk sizes: 1, 2, 4, ... up to head_chunk, head_chunk while heads
-  // remain, then halving again towards 1, so that the copies nothing can
-  // hide (the first chunk in, the last chunk out) are small.
-  std::vector<int> first;  // first head of each chunk, then BH
-  {
-    std::vector<int> up_sz, down_sz;
-    int left = BH;
-    for (int n = 1; n < L.hc && left > 0; n *= 2) {
-      const int a = n < left ? n : left;
-      up_sz.push_back(a);
-      left -= a;
-      if (left > 0) {
-        const int b = n < left ? n : left;
-        down_sz.push_back(b);
-        left -= b;
-      }
-    }
-    std::vector<int> mid;
-    while (left > 0) {
-      const int a = L.hc < left ? L.hc : left;
-      mid.push_back(a);
-      left -= a;
-    }
-    int h = 0;
-    for (int n : up_sz) first.push_back(h), h += n;
-    for (int n : mid) first.push_back(h), h += n;
-    for (auto it = down_sz.rbegin(); it != down_sz.rend(); ++it) first.push_back(h), h += *it;
-    first.push_back(h);
-  }
+  const std::vector<int> first = chunk_starts(B * H, L.hc);
   const int C = int(first.size()) - 1;
-  std::vector<cudaEvent_t> in_ready(C, nullptr), done(C, nullptr);
+  std::vector<cudaEvent_t> q_ready(C, nullptr), done(C, nullptr);
   cudaEvent_t start = nullptr, last = nullptr;
   sage_status st = SAGE_OK;
   auto fail = [&](sage_status s) {
@@ -149,17 +158,19 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     return e == cudaSuccess;
   };
   for (int c = 0; c < C && st == SAGE_OK; ++c) {
-    ck(cudaEventCreateWithFlags(&in_ready[c], cudaEventDisableTiming));
+    ck(cudaEventCreateWithFlags(&q_ready[c], cudaEventDisableTiming));
     ck(cudaEventCreateWithFlags(&done[c], cudaEventDisableTiming));
   }
   if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&last, cudaEventDisableTiming));
   if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&start, cudaEventDisableTiming));
-  // the copies start after everything already queued on the compute stream
-  // (e.g. a previous call that used the same workspace)
+  // the staging stream starts after everything already queued on the compute
+  // stream (e.g. a previous call that used the same workspace)
   if (st == SAGE_OK && ck(cudaEventRecord(start, cs))) ck(cudaStreamWaitEvent(xs, start, 0));
 
   const size_t qrow = size_t(Nq) * sg::kD * 2, krow = size_t(Nk) * sg::kD * 2;  // bytes per head
   auto heads_of = [&](int c) { return first[c + 1] - first[c]; };
+  auto q_strides = [&](int n) { return sage_strides{int64_t(n) * Nq * sg::kD, int64_t(Nq) * sg::kD, sg::kD}; };
+  auto kv_strides = [&](int n) { return sage_strides{int64_t(n) * Nk * sg::kD, int64_t(Nk) * sg::kD, sg::kD}; };
   auto h2d = [&](int c) {
     const int s = c & 1, n = heads_of(c);
     const size_t h0 = size_t(first[c]);
@@ -169,43 +180,51 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
                        cudaMemcpyHostToDevice, xs));
     ck(cudaMemcpyAsync(ws + L.off_in[s][2], static_cast<const uint8_t *>(v_host) + h0 * krow, n * krow,
                        cudaMemcpyHostToDevice, xs));
-    ck(cudaEventRecord(in_ready[c], xs));
   };
-  if (st == SAGE_OK) h2d(0);
-  if (st == SAGE_OK && C > 1) h2d(1);
+  // both quantizers of chunk c on the staging stream, then q_ready[c]
+  auto quantize = [&](int c) {
+    const int s = c & 1, n = heads_of(c);
+    sage_status r = sage_quantize_qk(ws + L.off_in[s][0], q_strides(n), ws + L.off_in[s][1], kv_strides(n), 1, n,
+                                     Nq, Nk, sg::kD, q_block, k_block, reinterpret_cast<int8_t *>(ws + L.off_qc[s]),
+                                     reinterpret_cast<float *>(ws + L.off_qs[s]),
+                                     reinterpret_cast<int8_t *>(ws + L.off_kc[s]),
+                                     reinterpret_cast<float *>(ws + L.off_ks[s]),
+                                     reinterpret_cast<float *>(ws + L.off_mu[s]), ws + L.off_wqk[s], L.wqk, xs);
+    if (r == SAGE_OK)
+      r = sage_quantize_v(ws + L.off_in[s][2], kv_strides(n), 1, n, Nk, sg::kD,
+                          reinterpret_cast<uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<float *>(ws + L.off_vs[s]),
+                          ws + L.off_wv[s], L.wv, xs);
+    if (r != SAGE_OK) fail(r);
+    else ck(cudaEventRecord(q_ready[c], xs));
+  };
+  for (int c = 0; c < 2 && c < C && st == SAGE_OK; ++c) {
+    h2d(c);
+    if (st == SAGE_OK) quantize(c);
+  }
   for (int c = 0; c < C && st == SAGE_OK; ++c) {
     const int s = c & 1, n = heads_of(c);
-    if (!ck(cudaStreamWaitEvent(cs, in_ready[c], 0))) break;
-    const sage_strides qs{int64_t(n) * Nq * sg::kD, int64_t(Nq) * sg::kD, sg::kD};
-    const sage_strides kvs{int64_t(n) * Nk * sg::kD, int64_t(Nk) * sg::kD, sg::kD};
-    auto *qc = reinterpret_cast<int8_t *>(ws + L.off_qc);
-    auto *kc = reinterpret_cast<int8_t *>(ws + L.off_kc);
-    auto *qsc = reinterpret_cast<float *>(ws + L.off_qs);
-    auto *ksc = reinterpret_cast<float *>(ws + L.off_ks);
-    auto *vc = reinterpret_cast<uint8_t *>(ws + L.off_vc);
-    auto *vsc = reinterpret_cast<float *>(ws + L.off_vs);
-    sage_status r = sage_quantize_qk(ws + L.off_in[s][0], qs, ws + L.off_in[s][1], kvs, 1, n, Nq, Nk, sg::kD,
-                                     q_block, k_block, qc, qsc, kc, ksc, reinterpret_cast<float *>(ws + L.off_mu),
-                                     ws + L.off_wqk, L.wqk, cs);
-    if (r == SAGE_OK)
-      r = sage_quantize_v(ws + L.off_in[s][2], kvs, 1, n, Nk, sg::kD, vc, vsc, ws + L.off_wv, L.wv, cs);
-    if (r == SAGE_OK)
-      r = sage_attn_fwd_ex(qc, qsc, kc, ksc, vc, vsc, 1, n, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal,
-                           ws + L.off_out[s], qs, nullptr, ws + L.off_wa, L.wa, status_dev, cs);
+    if (!ck(cudaStreamWaitEvent(cs, q_ready[c], 0))) break;
+    const sage_status r = sage_attn_fwd_ex(
+        reinterpret_cast<const int8_t *>(ws + L.off_qc[s]), reinterpret_cast<const float *>(ws + L.off_qs[s]),
+        reinterpret_cast<const int8_t *>(ws + L.off_kc[s]), reinterpret_cast<const float *>(ws + L.off_ks[s]),
+        reinterpret_cast<const uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<const float *>(ws + L.off_vs[s]), 1,
+        n, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal, ws + L.off_out[s], q_strides(n), nullptr,
+        ws + L.off_wa, L.wa, status_dev, cs);
     if (r != SAGE_OK) {
       fail(r);
       break;
     }
     if (!ck(cudaEventRecord(done[c], cs))) break;
-    if (!ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
+    if (c + 2 < C) h2d(c + 2);  // in[s] was last read by quantize(c), earlier on this stream
+    if (st != SAGE_OK || !ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
     ck(cudaMemcpyAsync(static_cast<uint8_t *>(out_host) + size_t(first[c]) * qrow, ws + L.off_out[s], n * qrow,
                        cudaMemcpyDeviceToHost, xs));
-    if (c + 2 < C) h2d(c + 2);
+    if (c + 2 < C && st == SAGE_OK) quantize(c + 2);
   }
   if (st == SAGE_OK && ck(cudaEventRecord(last, xs))) ck(cudaStreamWaitEvent(cs, last, 0));
   // events still pending on the device are released once they complete
   for (int c = 0; c < C; ++c) {
-    if (in_ready[c]) cudaEventDestroy(in_ready[c]);
+    if (q_ready[c]) cudaEventDestroy(q_ready[c]);
     if (done[c]) cudaEventDestroy(done[c]);
   }
   if (last) cudaEventDestroy(last);
