@@ -195,6 +195,26 @@ sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const
                              size_t workspace_bytes, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_attention - the dense path (sage_quantize_qk, sage_quantize_v,
+ * sage_attn_fwd_ex) in one call on device buffers, for callers that do not
+ * keep the codes: the three steps in a row on one stream, their
+ * intermediates in the workspace.  The result is bit for bit that of the
+ * three entry points called in a row.
+ *   q, k, v, out, strides, sizes, blocks, sm_scale, causal, lse: as in
+ *     sage_quantize_qk, sage_quantize_v and sage_attn_fwd_ex.
+ *   workspace: device memory of sage_attention_workspace(B, H, Nq, Nk)
+ *     bytes: codes, scales and means of all heads and the three entry
+ *     points' own workspaces.
+ * Errors as the three entry points, all checked before the first step is
+ * enqueued.
+ * ---------------------------------------------------------------------- */
+size_t sage_attention_workspace(int B, int H, int Nq, int Nk);
+sage_status sage_attention(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                           const void *v_bf16, sage_strides vs, int B, int H, int Nq, int Nk, int d, int q_block,
+                           int k_block, float sm_scale, int causal, void *out_bf16, sage_strides os, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/* ------------------------------------------------------------------------
  * sage_attention_host - the dense path (sage_quantize_qk, sage_quantize_v,
  * sage_attn_fwd_ex) on HOST buffers, with the host<->device copies and the
  * quantizers of one group of heads overlapped with the attention of another.

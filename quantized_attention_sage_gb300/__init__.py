@@ -9,7 +9,9 @@ been built (``build()``), every call raises.
 
 Entry points (same names as the C ABI):
   sage_quantize_qk, sage_quantize_v, sage_attn_fwd, int8kv_prompt_attn
-plus ``sage_attention`` (the three dense steps in a row).
+plus ``sage_attention`` (the three dense steps in one call) and ``sage_attention_host`` (the
+same on host buffers, with the copies and quantizers of one group of heads overlapped with the
+attention of another).
 """
 
 from __future__ import annotations
@@ -89,6 +91,11 @@ def lib():
     L.sage_attention_host.restype = i32
     L.sage_attention_host.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, i32, vp, sz, vp,
                                       vp, vp]
+    L.sage_attention_workspace.restype = sz
+    L.sage_attention_workspace.argtypes = [i32, i32, i32, i32]
+    L.sage_attention.restype = i32
+    L.sage_attention.argtypes = [vp, Strides, vp, Strides, vp, Strides, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                 vp, Strides, vp, vp, sz, vp, vp]
     L.sage_attn_fwd_ex.restype = i32
     L.sage_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                    vp, Strides, vp, vp, sz, vp, vp]
@@ -300,16 +307,42 @@ def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: in
     return int(status.item())
 
 
-def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,
-                   stream=None, causal: bool = False, return_lse: bool = False):
-    """The dense path in one call: quantize Q/K, quantize V, attention."""
-    qk = sage_quantize_qk(q, k, q_block, k_block, stream=stream)
-    vq = sage_quantize_v(v, stream=stream)
-    return sage_attn_fwd(qk, vq, q_block, k_block, sm_scale, out=out, stream=stream, causal=causal,
-                         return_lse=return_lse)
-
-
 _copy_streams = {}
+
+
+def _side_stream(cache: dict, dev):
+    s = cache.get(dev.index)
+    if s is None:
+        s = cache[dev.index] = _torch().cuda.Stream(device=dev)
+    return s
+
+
+def sage_attention(q, k, v, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,
+                   stream=None, causal: bool = False, return_lse: bool = False, workspace=None, status=None):
+    """The dense path in one call (C ``sage_attention``): quantize Q/K, quantize V, attention.
+
+    q: [B,H,Nq,128], k, v: [B,H,Nk,128] bf16 CUDA tensors (16-byte aligned strides).
+    Returns out bf16 [B,H,Nq,128], or (out, lse) with ``return_lse``."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, torch.bfloat16, name, 4)
+    if (q.shape[:2] != k.shape[:2] or k.shape != v.shape or q.shape[3] != D or k.shape[3] != D
+            or not (q.device == k.device == v.device)):
+        raise ValueError("q [B,H,Nq,128], k and v [B,H,Nk,128] on one device")
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev) if return_lse else None
+    L = lib()
+    nbytes = L.sage_attention_workspace(B, H, Nq, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_attention(_ptr(q), _strides4(q), _ptr(k), _strides4(k), _ptr(v), _strides4(v), B, H, Nq, Nk, D,
+                            q_block, k_block, float(sm_scale), int(bool(causal)), _ptr(out), _strides4(out),
+                            _ptr(lse), _ptr(ws), nbytes, _ptr(status), _stream(stream)),
+           "sage_attention")
+    return (out, lse) if return_lse else out
 
 
 def sage_attention_host(q, k, v, out, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0,
@@ -328,9 +361,7 @@ def sage_attention_host(q, k, v, out, q_block: int = 64, k_block: int = 64, sm_s
     Nk = k.shape[2]
     dev = torch.device("cuda", torch.cuda.current_device())
     if copy_stream is None:
-        copy_stream = _copy_streams.get(dev.index)
-        if copy_stream is None:
-            copy_stream = _copy_streams[dev.index] = torch.cuda.Stream(device=dev)
+        copy_stream = _side_stream(_copy_streams, dev)
     L = lib()
     nbytes = L.sage_attention_host_workspace(B, H, Nq, Nk, head_chunk)
     ws = _workspace(nbytes, dev, workspace)

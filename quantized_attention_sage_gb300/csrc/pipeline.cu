@@ -116,9 +116,86 @@ std::vector<int> chunk_starts(int BH, int hc) {
   return first;
 }
 
+// sage_attention: the same three steps on device buffers in one call.  The
+// intermediates of all heads live in the caller's workspace.
+struct DeviceLayout {
+  size_t off_qc, off_kc, off_qs, off_ks, off_mu, off_vc, off_vs, off_wqk, off_wv, off_wa;
+  size_t wqk, wv, wa, total;
+};
+
+DeviceLayout device_layout(int B, int H, int Nq, int Nk) {
+  DeviceLayout L{};
+  const size_t BH = size_t(B) * H;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += up(bytes);
+    return o;
+  };
+  L.off_qc = take(BH * Nq * sg::kD);
+  L.off_kc = take(BH * Nk * sg::kD);
+  L.off_qs = take(BH * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
+  L.off_ks = take(BH * sg::ceil_div(Nk, 64) * sizeof(float));
+  L.off_mu = take(BH * sg::kD * sizeof(float));
+  L.off_vc = take(BH * sg::kD * size_t(sg::nk_pad(Nk)));
+  L.off_vs = take(BH * sg::kD * sizeof(float));
+  L.wqk = sage_quantize_qk_workspace(B, H, Nk);
+  L.wv = sage_quantize_v_workspace(B, H, Nk);
+  L.wa = sage_attn_fwd_workspace(B, H, Nq, Nk);
+  L.off_wqk = take(L.wqk);
+  L.off_wv = take(L.wv);
+  L.off_wa = take(L.wa);
+  L.total = off + kAlign;  // room to align the base
+  return L;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t sage_attention_workspace(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+  return device_layout(B, H, Nq, Nk).total;
+}
+
+sage_status sage_attention(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                           const void *v_bf16, sage_strides vs, int B, int H, int Nq, int Nk, int d, int q_block,
+                           int k_block, float sm_scale, int causal, void *out_bf16, sage_strides os, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t *status_dev, void *stream) {
+  // every argument is checked here, before the first step is enqueued
+  if (d != sg::kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || int64_t(B) * H > 65535 || Nq > (1 << 28) || Nk > (1 << 28))
+    return SAGE_ERR_INVALID_ARG;
+  auto a16 = [](const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  auto s16 = [](const sage_strides &t) {  // element strides of bf16 rows: 16-byte multiples
+    return t.b >= 0 && t.h >= 0 && t.n >= 0 && t.b % 8 == 0 && t.h % 8 == 0 && t.n % 8 == 0;
+  };
+  if (!a16(q_bf16) || !a16(k_bf16) || !a16(v_bf16) || !a16(out_bf16) || workspace == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  if (!s16(qs) || !s16(ks) || !s16(vs) || !s16(os)) return SAGE_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SAGE_ERR_INVALID_ARG;
+  const DeviceLayout L = device_layout(B, H, Nq, Nk);
+  if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
+  uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + kAlign - 1) &
+                                            ~uintptr_t(kAlign - 1));
+  auto *qc = reinterpret_cast<int8_t *>(ws + L.off_qc);
+  auto *kc = reinterpret_cast<int8_t *>(ws + L.off_kc);
+  auto *qsc = reinterpret_cast<float *>(ws + L.off_qs);
+  auto *ksc = reinterpret_cast<float *>(ws + L.off_ks);
+  auto *vc = reinterpret_cast<uint8_t *>(ws + L.off_vc);
+  auto *vsc = reinterpret_cast<float *>(ws + L.off_vs);
+  sage_status r = sage_quantize_qk(q_bf16, qs, k_bf16, ks, B, H, Nq, Nk, sg::kD, q_block, k_block, qc, qsc, kc, ksc,
+                                   reinterpret_cast<float *>(ws + L.off_mu), ws + L.off_wqk, L.wqk, stream);
+  if (r == SAGE_OK)
+    r = sage_quantize_v(v_bf16, vs, B, H, Nk, sg::kD, vc, vsc, ws + L.off_wv, L.wv, stream);
+  if (r == SAGE_OK)
+    r = sage_attn_fwd_ex(qc, qsc, kc, ksc, vc, vsc, B, H, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal,
+                         out_bf16, os, lse, ws + L.off_wa, L.wa, status_dev, stream);
+  return r;
+}
 
 size_t sage_attention_host_workspace(int B, int H, int Nq, int Nk, int head_chunk) {
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || head_chunk < 1) return 0;

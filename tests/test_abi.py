@@ -185,3 +185,23 @@ def test_binding_rejects_wrong_dtypes_and_host_tensors():
         qas.sage_attn_fwd(qk, vq)
     with pytest.raises(ValueError, match="int8"):
         qas.sage_attn_fwd(dict(qk, q_codes=qk["q_codes"].to(torch.uint8)), vq)
+
+
+def test_one_call_dense_path_rejects_bad_arguments(L):
+    ws = L.sage_attention_workspace(1, 24, 256, 256)
+    assert ws > 24 * 256 * 128 * 3
+    assert L.sage_attention_workspace(1, 24, 0, 256) == 0
+    st = s4(24 * 256 * 128, 256 * 128, 128)
+
+    def call(d=128, qb=64, causal=0, Nq=256, Nk=256, q=FAKE, qs=st, lse=None, wsb=ws):
+        return L.sage_attention(q, qs, FAKE, st, FAKE, st, 1, 24, Nq, Nk, d, qb, 64, 0.0, causal, FAKE, st, lse,
+                                FAKE, wsb, None, None)
+    assert call(d=96) == 2
+    assert call(qb=32) == 2
+    assert call(causal=2) == 1
+    assert call(causal=1, Nq=300) == 2      # causal needs Nq <= Nk
+    assert call(q=None) == 1
+    assert call(q=FAKE + 8) == 1            # 16-byte aligned rows only
+    assert call(qs=s4(24 * 256 * 128, 256 * 128, 132)) == 1
+    assert call(lse=FAKE + 2) == 1
+    assert call(wsb=ws - 1) == 4

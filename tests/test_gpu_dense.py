@@ -27,6 +27,13 @@ def run_dense(qas, q, k, v, bq, bk):
     return qk, vq, out
 
 
+def three_calls(qas, q, k, v, bq, bk, causal=False, return_lse=False):
+    """The dense path as its three entry points called in a row on one stream."""
+    qk = qas.sage_quantize_qk(q, k, bq, bk)
+    vq = qas.sage_quantize_v(v)
+    return qas.sage_attn_fwd(qk, vq, bq, bk, causal=causal, return_lse=return_lse)
+
+
 def check_head(qk, vq, out, b, h, qbits, kbits, vbits, bq, bk, rows=None, tag=""):
     ref = oracle.sage_head(qbits, kbits, vbits, bq, bk, rows=rows)
     assert np.array_equal(qk["k_mean"][b, h].cpu().numpy(), ref["mu"]), f"{tag} k_mean"
@@ -242,7 +249,7 @@ def test_host_pipeline_equals_the_device_path(cuda_lib, B, H, nq, nk, chunk, cau
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
 
     hq, hk, hv = host(x["q"]), host(x["k"]), host(x["v"])
-    ref = cuda_lib.sage_attention(hq.cuda(), hk.cuda(), hv.cuda(), 64, 64, causal=causal)
+    ref = three_calls(cuda_lib, hq.cuda(), hk.cuda(), hv.cuda(), 64, 64, causal=causal)
     side = torch.cuda.Stream()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = torch.empty(cuda_lib.lib().sage_attention_host_workspace(B, H, nq, nk, chunk), dtype=torch.uint8,
@@ -288,3 +295,30 @@ def test_dense_long_sequence_sampled(cuda_lib):
     qk, vq, out = run_dense(cuda_lib, bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"]), 128, 128)
     rows = np.array([0, 1, 4095, 100000, 131071, 200002])
     check_head(qk, vq, out, 0, 0, x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], 128, 128, rows=rows, tag="long")
+
+
+@pytest.mark.parametrize("B,H,nq,nk,causal,token_major", [(1, 24, 300, 300, False, False),
+                                                          (1, 2, 129, 200, True, False),
+                                                          (3, 2, 257, 257, False, False),
+                                                          (2, 5, 190, 321, False, True)])
+def test_one_call_equals_the_three_entry_points(cuda_lib, B, H, nq, nk, causal, token_major):
+    """sage_attention (the three steps in one call, intermediates in its workspace)
+    gives the bits of the three entry points in a row, output and lse, also on
+    token-major strided views; two calls share the workspace."""
+    w = synth.DenseWorkload(f"one_{B}_{H}_{nq}_{nk}", 17, B, H, nq, nk, 64, sub=(nq + 3 * nk) % 89)
+    x = synth.dense_inputs(w)
+    if token_major:  # [B, N, H, 128] storage viewed as [B, H, N, 128]
+        q, k, v = (bf16_dev(np.ascontiguousarray(x[t].transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+                   for t in ("q", "k", "v"))
+    else:
+        q, k, v = bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"])
+    ref, ref_lse = three_calls(cuda_lib, q, k, v, 64, 128, causal=causal, return_lse=True)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(cuda_lib.lib().sage_attention_workspace(B, H, nq, nk), dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        out, lse = cuda_lib.sage_attention(q, k, v, 64, 128, causal=causal, return_lse=True, status=status,
+                                           workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {rep}"
+        assert torch.equal(lse, ref_lse), f"call {rep} lse"
+    assert status.item() == 0
