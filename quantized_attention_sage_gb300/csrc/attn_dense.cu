@@ -15,7 +15,8 @@
 //  * Q, K (fp16 images) and V^T (E4M3) tiles arrive by TMA into 128-byte
 //    swizzled shared memory; S (double-buffered) and O live in TMEM.
 //  * One CTA owns two 128-row query tiles of one (b, h); every K/V tile read
-//    serves both.  Warp 0 issues TMA; warps 1 and 3 issue Q.K^T of tile 0
+//    serves both.  (When the last wave of CTAs would leave more than half of
+//    the SMs idle, its pairs run as single-tile CTAs instead.)  Warp 0 issues TMA; warps 1 and 3 issue Q.K^T of tile 0
 //    and tile 1, warp 2 issues both P.V (tcgen05.mma issue blocks for about
 //    one MMA's execution and slows the softmax warps of the issuing
 //    sub-partition, so the issue is spread); warps 4-7 and 8-11 are two
@@ -78,6 +79,8 @@ struct Params {
   float *lse;        // per-row log-sum-exp [B*H][Nq] (natural base), or null
   uint64_t wait_ns;  // limit of every bounded wait
   int fault;         // test hook: 1 = the producer issues no loads, so waits run out
+  int pairs;         // query-tile pairs per head
+  int n_pairs;       // 1-D grid: the first n_pairs CTAs take pairs, the rest single tiles; -1: 2-D grid
 };
 
 struct Bars {
@@ -105,11 +108,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  // causal: the CTAs with the most key tiles (the last query rows) start first
-  const int qpair = p.causal ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
-  const int q0 = qpair * 2 * BM;
-  const int ntile = (q0 + BM < p.Nq) ? 2 : 1;  // second query tile present?
+  int bh, q0, ntile;
+  if (p.n_pairs >= 0) {
+    // last-wave balancing: pairs of query tiles in (head, pair) order, then the
+    // tiles of the remaining pairs one per CTA, so that the last wave spreads
+    // over twice as many SMs
+    const int u = blockIdx.x;
+    if (u < p.n_pairs) {
+      bh = u / p.pairs;
+      q0 = (u - bh * p.pairs) * 2 * BM;
+      ntile = (q0 + BM < p.Nq) ? 2 : 1;
+    } else {
+      const int v = u - p.n_pairs, g = p.n_pairs + (v >> 1);
+      bh = g / p.pairs;
+      q0 = (g - bh * p.pairs) * 2 * BM + (v & 1) * BM;
+      ntile = 1;
+    }
+  } else {
+    bh = blockIdx.y;
+    // causal: the CTAs with the most key tiles (the last query rows) start first
+    const int qpair = p.causal ? int(gridDim.x) - 1 - int(blockIdx.x) : int(blockIdx.x);
+    q0 = qpair * 2 * BM;
+    ntile = (q0 + BM < p.Nq) ? 2 : 1;  // second query tile present?
+  }
+  if (q0 >= p.Nq) return;  // the second tile of a ragged last pair: nothing to do
   const int coff = p.Nk - p.Nq;                 // causal offset: row i sees keys <= i + coff
   const int T = p.causal ? (min(q0 + ntile * BM, p.Nq) - 1 + coff) / BN + 1 : ceil_div(p.Nk, BN);
 
@@ -578,6 +600,21 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   e = set_smem_attr_once(reinterpret_cast<const void *>(sage_attn_fwd_kernel), kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(ceil_div(a.Nq, 2 * BM), BH);
+  p.pairs = ceil_div(a.Nq, 2 * BM);
+  p.n_pairs = -1;
+  {
+    // Equal CTAs fill whole waves of one CTA per SM; when the last wave is at
+    // most half full, its pairs are split into single-tile CTAs (a single tile
+    // takes ~0.8 of a pair's time, measured), which shortens the tail.
+    // Causal CTAs are unequal and keep the longest-first 2-D order.
+    const long long total = (long long)BH * p.pairs;
+    const int sms = current_sm_count();
+    const int rem = sms > 0 ? int(total % sms) : 0;
+    if (!a.causal && total > sms && rem > 0 && 2 * rem <= sms) {
+      p.n_pairs = int(total - rem);
+      grid = dim3(unsigned(p.n_pairs + 2 * rem), 1);
+    }
+  }
   sage_attn_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -322,3 +322,16 @@ def test_one_call_equals_the_three_entry_points(cuda_lib, B, H, nq, nk, causal, 
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"call {rep}"
         assert torch.equal(lse, ref_lse), f"call {rep} lse"
     assert status.item() == 0
+
+
+def test_dense_last_wave_single_tile_ctas(cuda_lib):
+    """One head of 41,372 tokens: 162 pairs of query tiles, so on 152 SMs the last
+    10 pairs run as 20 single-tile CTAs, the very last one past Nq (it returns at
+    once).  Rows on both sides of the switch and of every converted tile's border
+    against the oracle."""
+    n = 162 * 256 - 100
+    w = synth.DenseWorkload("tail_wave", 18, 1, 1, n, n, 128, sub=2)
+    x = synth.dense_inputs(w)
+    qk, vq, out = run_dense(cuda_lib, bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"]), 128, 128)
+    rows = np.array([0, 38911, 38912, 39039, 39040, 39167, 41215, 41216, 41343, n - 1])
+    check_head(qk, vq, out, 0, 0, x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], 128, 128, rows=rows, tag="tail")
