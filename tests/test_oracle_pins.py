@@ -7,6 +7,7 @@ fails here.  No expected value comes from the CUDA library.
 """
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -522,3 +523,26 @@ def test_causal_first_row_is_the_dequantised_first_v_row_and_its_lse():
     t = np.float32(np.float32(sq[0] * sk[0]) * C)
     s00 = np.float32(np.float32(int(qc[0].astype(np.int64) @ kc[0].astype(np.int64))) * t)
     assert lse[0] == pytest.approx(math.log(2.0) * float(s00), rel=1e-15)
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)):
+        line = line.split("|")[0].strip()
+        if line and not line.startswith("#"):
+            key, val = (s.strip() for s in line.split("="))
+            vals[key] = int(val)
+    return vals
+
+
+def test_workloads_match_the_sizes_the_pages_print():
+    """The synthetic stand-ins have the sizes the pages measure on (golden fixture
+    with citations): the 37,810-token dense self-attention and the int8-KV prompt
+    chunks 32K x 1024 and 64K x 512."""
+    g = _golden("page_workloads.txt")
+    w = synth.dense_workload("videodit_b1h24n37810")
+    assert w.Nq == w.Nk == g["dense.tokens"]
+    a = synth.int8kv_workload("prompt32k_q1024")
+    assert (a.Nk, a.Nq) == (g["int8kv.context_32k"], g["int8kv.queries_32k"])
+    b = synth.int8kv_workload("prompt64k_q512_outliers")
+    assert (b.Nk, b.Nq) == (g["int8kv.context_64k"], g["int8kv.queries_64k"])
