@@ -363,15 +363,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
         if (!ok) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + kColO + 32 * c, o);
-          tmem_ld_wait(o);
+        // one load round trip and one store round trip for the 128 columns
+        uint32_t o[128];
+        tmem_ld32(lane_base + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_ld32(lane_base + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tmem_ld32(lane_base + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+        tmem_ld32(lane_base + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
+        tmem_ld_wait(o);
+        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__fmul_rn(alpha, __uint_as_float(o[i])));
-          tmem_st32(lane_base + kColO + 32 * c, o);
+        for (int i = 0; i < 128; i += 2) {
+          const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+          o[i] = __float_as_uint(v.x);
+          o[i + 1] = __float_as_uint(v.y);
         }
+        tmem_st32(lane_base + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_st32(lane_base + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tmem_st32(lane_base + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
+        tmem_st32(lane_base + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
       }
       tmem_st_wait();
       tc_fence_before();
