@@ -52,7 +52,7 @@ WORKLOAD = "videodit_b1h24n37810"
 # 8192-token case scaled by 37810/8192 (every head's inputs are read once, so
 # the bytes grow with heads x tokens), for the kernel source with this sha256
 # prefix; None once the source has changed.
-TRAFFIC = {"sha256_prefix": "82d604f39018e2a2", "bytes": 925.3e6}
+TRAFFIC = {"sha256_prefix": "8c5862e9f02ab6e1", "bytes": 929.3e6}
 
 
 def peaks():
@@ -344,7 +344,8 @@ def run_ours(args, rank, world):
         qas.sage_attention_host(hq, hk, hv, hout, bq, bk, head_chunk=head_chunk, workspace=ws_host, status=status,
                                 stream=cstream, copy_stream=xstream)
 
-    e2e_step()
+    for _ in range(max(3, args.warmup)):  # warm-up, as for the device steps
+        e2e_step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)

@@ -558,10 +558,13 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   using namespace dense;
   const int BH = a.B * a.H;
   const int64_t nq = int64_t(BH) * a.Nq * kD, nk = int64_t(BH) * a.Nk * kD;
-  cudaError_t e = launch_codes_to_f16(a.q_codes, a.q_img, nq, st);
-  if (e != cudaSuccess) return e;
-  e = launch_codes_to_f16(a.k_codes, a.k_img, nk, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (!a.images_ready) {
+    e = launch_codes_to_f16(a.q_codes, a.q_img, nq, st);
+    if (e != cudaSuccess) return e;
+    e = launch_codes_to_f16(a.k_codes, a.k_img, nk, st);
+    if (e != cudaSuccess) return e;
+  }
 
   CUtensorMap tq, tk, tv;
   const int npad = nk_pad(a.Nk);

@@ -57,9 +57,12 @@ struct DenseArgs {
   int fault = 0;                     // test hook (see sage_attn_fwd_fault_test)
   int causal = 0;                    // query i sees keys j <= i + (Nk - Nq)
   float *lse = nullptr;              // per-row log-sum-exp [B*H][Nq], or null
+  bool images_ready = false;         // q_img / k_img already hold the images (no conversion launches)
 };
 size_t dense_workspace_bytes(int B, int H, int Nq, int Nk);
 cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st);
+// exact fp16 images of n int8 codes (16-byte aligned, n a multiple of 16)
+cudaError_t launch_codes_to_f16(const int8_t *codes, void *img, int64_t n, cudaStream_t st);
 
 // int8 KV-cache prompt attention (attn_int8kv.cu)
 struct Int8KVArgs {

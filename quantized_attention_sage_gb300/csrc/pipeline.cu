@@ -7,21 +7,22 @@
 // the end, so that the first copy in and the last copy out are short).  Two
 // streams share the work:
 //   staging stream (the caller's copy stream): host->device copies, the two
-//            quantizers, device->host copies;
-//   compute stream: the attention of one chunk after another.
+//            quantizers and the fp16 images of the Q/K codes, device->host
+//            copies;
+//   compute stream: the attention kernel of one chunk after another.
 // While the compute stream attends chunk c, the staging stream copies chunk
 // c+2 in, then (once chunk c is done) copies its output out and quantizes
 // chunk c+2, so that neither the copies nor the short quantizer launches
 // sit between two attention launches.  Inputs, outputs and the quantized
-// intermediates are double-buffered in the caller's workspace (slot c % 2);
-// the attention workspace is single-buffered because only the compute stream
-// touches it.  Cross-stream order comes from events created for the call
+// intermediates (codes, scales, images) are double-buffered in the caller's
+// workspace (slot c % 2).  Cross-stream order comes from events created for the call
 // (timing disabled) and released as soon as they are enqueued.
 //
 // Per chunk c (slot s = c % 2), in stream order:
-//   staging: H2D q, k, v -> in[s]; quantize in[s] -> codes[s]; record q_ready[c]
+//   staging: H2D q, k, v -> in[s]; quantize in[s] -> codes[s], images[s];
+//            record q_ready[c]
 //   compute: wait q_ready[c]; attention codes[s] -> out[s]; record done[c]
-//   staging: wait done[c]; D2H out[s]; quantize chunk c+2 into codes[s]
+//   staging: wait done[c]; D2H out[s]; quantize chunk c+2 into codes[s], images[s]
 // H2D of chunk c+2 is queued before the wait for done[c]: in[s] was last read
 // by the quantizers of chunk c, earlier on the same stream.  The quantizers
 // of chunk c+2 follow done[c] (codes[s] has been read) and D2H of chunk c
@@ -31,6 +32,7 @@
 // synchronises one stream.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <vector>
 
 #include "internal.h"
@@ -46,8 +48,8 @@ struct HostLayout {
   size_t q_bytes, k_bytes, o_bytes;     // bf16 chunk buffers
   size_t off_in[2][3], off_out[2];      // inputs (q, k, v) and output per slot
   size_t off_qc[2], off_kc[2], off_qs[2], off_ks[2], off_mu[2], off_vc[2], off_vs[2], off_wqk[2], off_wv[2];
-  size_t off_wa;                        // attention workspace (compute stream only)
-  size_t wqk, wv, wa, total;
+  size_t off_qi[2], off_ki[2];          // fp16 images of the Q and K codes the attention reads
+  size_t wqk, wv, total;
 };
 
 HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
@@ -60,7 +62,6 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
   L.o_bytes = L.q_bytes;
   L.wqk = sage_quantize_qk_workspace(1, L.hc, Nk);
   L.wv = sage_quantize_v_workspace(1, L.hc, Nk);
-  L.wa = sage_attn_fwd_workspace(1, L.hc, Nq, Nk);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -81,8 +82,9 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
     L.off_vs[s] = take(hc * sg::kD * sizeof(float));
     L.off_wqk[s] = take(L.wqk);
     L.off_wv[s] = take(L.wv);
+    L.off_qi[s] = take(hc * Nq * sg::kD * 2);
+    L.off_ki[s] = take(hc * Nk * sg::kD * 2);
   }
-  L.off_wa = take(L.wa);
   L.total = off + kAlign;  // room to align the base
   return L;
 }
@@ -271,8 +273,16 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
       r = sage_quantize_v(ws + L.off_in[s][2], kv_strides(n), 1, n, Nk, sg::kD,
                           reinterpret_cast<uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<float *>(ws + L.off_vs[s]),
                           ws + L.off_wv[s], L.wv, xs);
-    if (r != SAGE_OK) fail(r);
-    else ck(cudaEventRecord(q_ready[c], xs));
+    if (r != SAGE_OK) {
+      fail(r);
+      return;
+    }
+    // the attention's fp16 images of the codes, so that only its kernel runs on the compute stream
+    ck(sg::launch_codes_to_f16(reinterpret_cast<const int8_t *>(ws + L.off_qc[s]), ws + L.off_qi[s],
+                               int64_t(n) * Nq * sg::kD, xs));
+    ck(sg::launch_codes_to_f16(reinterpret_cast<const int8_t *>(ws + L.off_kc[s]), ws + L.off_ki[s],
+                               int64_t(n) * Nk * sg::kD, xs));
+    if (st == SAGE_OK) ck(cudaEventRecord(q_ready[c], xs));
   };
   for (int c = 0; c < 2 && c < C && st == SAGE_OK; ++c) {
     h2d(c);
@@ -281,16 +291,29 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
   for (int c = 0; c < C && st == SAGE_OK; ++c) {
     const int s = c & 1, n = heads_of(c);
     if (!ck(cudaStreamWaitEvent(cs, q_ready[c], 0))) break;
-    const sage_status r = sage_attn_fwd_ex(
-        reinterpret_cast<const int8_t *>(ws + L.off_qc[s]), reinterpret_cast<const float *>(ws + L.off_qs[s]),
-        reinterpret_cast<const int8_t *>(ws + L.off_kc[s]), reinterpret_cast<const float *>(ws + L.off_ks[s]),
-        reinterpret_cast<const uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<const float *>(ws + L.off_vs[s]), 1,
-        n, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal, ws + L.off_out[s], q_strides(n), nullptr,
-        ws + L.off_wa, L.wa, status_dev, cs);
-    if (r != SAGE_OK) {
-      fail(r);
-      break;
-    }
+    // the attention kernel alone (arguments checked above; images written by the staging stream)
+    sg::DenseArgs a;
+    a.q_codes = reinterpret_cast<const int8_t *>(ws + L.off_qc[s]);
+    a.q_scales = reinterpret_cast<const float *>(ws + L.off_qs[s]);
+    a.k_codes = reinterpret_cast<const int8_t *>(ws + L.off_kc[s]);
+    a.k_scales = reinterpret_cast<const float *>(ws + L.off_ks[s]);
+    a.v_codes = reinterpret_cast<const uint8_t *>(ws + L.off_vc[s]);
+    a.v_scales = reinterpret_cast<const float *>(ws + L.off_vs[s]);
+    a.B = 1;
+    a.H = n;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.q_block = q_block;
+    a.k_block = k_block;
+    a.sm_scale = sm_scale > 0.f ? sm_scale : float(1.0 / std::sqrt(double(sg::kD)));
+    a.out = ws + L.off_out[s];
+    a.os = q_strides(n);
+    a.q_img = ws + L.off_qi[s];
+    a.k_img = ws + L.off_ki[s];
+    a.status = status_dev;
+    a.causal = causal;
+    a.images_ready = true;
+    if (!ck(sg::launch_attn_dense(a, cs))) break;
     if (!ck(cudaEventRecord(done[c], cs))) break;
     if (c + 2 < C) h2d(c + 2);  // in[s] was last read by quantize(c), earlier on this stream
     if (st != SAGE_OK || !ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
