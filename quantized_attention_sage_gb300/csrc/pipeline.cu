@@ -15,13 +15,14 @@
 // chunk c+2, so that neither the copies nor the short quantizer launches
 // sit between two attention launches.  Inputs, outputs and the quantized
 // intermediates (codes, scales, images) are double-buffered in the caller's
-// workspace (slot c % 2).  Cross-stream order comes from events created for the call
-// (timing disabled) and released as soon as they are enqueued.
+// workspace (slot c % 2).  Cross-stream order comes from events created for
+// the call (timing disabled) and released as soon as they are enqueued.
 //
 // Per chunk c (slot s = c % 2), in stream order:
 //   staging: H2D q, k, v -> in[s]; quantize in[s] -> codes[s], images[s];
 //            record q_ready[c]
-//   compute: wait q_ready[c]; attention codes[s] -> out[s]; record done[c]
+//   compute: wait q_ready[c]; attention kernel on codes[s], images[s] -> out[s];
+//            record done[c]
 //   staging: wait done[c]; D2H out[s]; quantize chunk c+2 into codes[s], images[s]
 // H2D of chunk c+2 is queued before the wait for done[c]: in[s] was last read
 // by the quantizers of chunk c, earlier on the same stream.  The quantizers
