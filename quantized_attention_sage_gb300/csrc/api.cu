@@ -68,19 +68,7 @@ namespace {
 
 constexpr int kAbiVersion = 1;
 
-bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-bool strides_ok(const sage_strides &s) {
-  return s.b >= 0 && s.h >= 0 && s.n >= 0 && (s.b % 8) == 0 && (s.h % 8) == 0 && (s.n % 8) == 0;
-}
-
-bool sizes_ok(int B, int H, int N) {
-  return B >= 1 && H >= 1 && N >= 1 && int64_t(B) * H <= 65535 && N <= (1 << 28);
-}
-
 sage_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
-
-float default_scale(float sm_scale) { return sm_scale > 0.f ? sm_scale : float(1.0 / std::sqrt(128.0)); }
 
 }  // namespace
 

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 
@@ -23,6 +24,20 @@ int current_sm_count();
 // would leave a second device without it.
 cudaError_t set_smem_attr_once(const void *kernel, int bytes, unsigned long long *done_mask);
 __host__ __device__ inline int nk_pad(int nk) { return ceil_div(nk, kTile) * kTile; }
+
+// Host-side argument checks shared by the entry points.
+// A non-null pointer on a 16-byte boundary (TMA and vector accesses).
+inline bool aligned16(const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Element strides of bf16 rows that keep every row on a 16-byte boundary.
+inline bool strides_ok(const sage_strides &s) {
+  return s.b >= 0 && s.h >= 0 && s.n >= 0 && (s.b % 8) == 0 && (s.h % 8) == 0 && (s.n % 8) == 0;
+}
+// Problem sizes the grids and 32-bit index arithmetic support.
+inline bool sizes_ok(int B, int H, int N) {
+  return B >= 1 && H >= 1 && N >= 1 && int64_t(B) * H <= 65535 && N <= (1 << 28);
+}
+// sm_scale <= 0 selects 1/sqrt(d).
+inline float default_scale(float sm_scale) { return sm_scale > 0.f ? sm_scale : float(1.0 / std::sqrt(double(kD))); }
 
 // quantisers (quant.cu)
 cudaError_t launch_quantize_qk(const void *q, sage_strides qs, const void *k, sage_strides ks, int B, int H,

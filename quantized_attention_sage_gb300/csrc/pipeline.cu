@@ -33,7 +33,6 @@
 // synchronises one stream.
 #include <cuda_runtime.h>
 
-#include <cmath>
 #include <vector>
 
 #include "internal.h"
@@ -170,15 +169,12 @@ sage_status sage_attention(const void *q_bf16, sage_strides qs, const void *k_bf
   if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
   if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || int64_t(B) * H > 65535 || Nq > (1 << 28) || Nk > (1 << 28))
+  if (!sg::sizes_ok(B, H, Nq) || !sg::sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!sg::aligned16(q_bf16) || !sg::aligned16(k_bf16) || !sg::aligned16(v_bf16) || !sg::aligned16(out_bf16) ||
+      workspace == nullptr)
     return SAGE_ERR_INVALID_ARG;
-  auto a16 = [](const void *p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  auto s16 = [](const sage_strides &t) {  // element strides of bf16 rows: 16-byte multiples
-    return t.b >= 0 && t.h >= 0 && t.n >= 0 && t.b % 8 == 0 && t.h % 8 == 0 && t.n % 8 == 0;
-  };
-  if (!a16(q_bf16) || !a16(k_bf16) || !a16(v_bf16) || !a16(out_bf16) || workspace == nullptr)
+  if (!sg::strides_ok(qs) || !sg::strides_ok(ks) || !sg::strides_ok(vs) || !sg::strides_ok(os))
     return SAGE_ERR_INVALID_ARG;
-  if (!s16(qs) || !s16(ks) || !s16(vs) || !s16(os)) return SAGE_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SAGE_ERR_INVALID_ARG;
   const DeviceLayout L = device_layout(B, H, Nq, Nk);
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
@@ -213,9 +209,7 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
   if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
   if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
   if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || head_chunk < 1 || int64_t(B) * H > 65535 || Nq > (1 << 28) ||
-      Nk > (1 << 28))
-    return SAGE_ERR_INVALID_ARG;
+  if (!sg::sizes_ok(B, H, Nq) || !sg::sizes_ok(B, H, Nk) || head_chunk < 1) return SAGE_ERR_INVALID_ARG;
   if (q_host == nullptr || k_host == nullptr || v_host == nullptr || out_host == nullptr || workspace == nullptr)
     return SAGE_ERR_INVALID_ARG;
   if (copy_stream == nullptr || copy_stream == compute_stream) return SAGE_ERR_INVALID_ARG;
@@ -306,7 +300,7 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     a.Nk = Nk;
     a.q_block = q_block;
     a.k_block = k_block;
-    a.sm_scale = sm_scale > 0.f ? sm_scale : float(1.0 / std::sqrt(double(sg::kD)));
+    a.sm_scale = sg::default_scale(sm_scale);
     a.out = ws + L.off_out[s];
     a.os = q_strides(n);
     a.q_img = ws + L.off_qi[s];
