@@ -429,6 +429,11 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
                                                           float *__restrict__ kt, float *__restrict__ vsf,
                                                           uint32_t *__restrict__ vmax_bits) {
   __shared__ uint32_t vw[BN][kD / 4];  // the V tile's codes, key-major, 4 codes per word
+  // the tile's fp16 images, channel-major; the 16-byte chunk of keys 8q..8q+7
+  // of channel ch sits at chunk q ^ ((ch >> 2) & 15) of its row, so that the
+  // transposing writes (one channel quad per lane) and the row reads below
+  // spread over the banks
+  __shared__ uint4 vt[kD][BN / 8];
   const int tile = blockIdx.x, g = blockIdx.y;
   const int key0 = tile * BN;
   const int8_t *ksrc = kc + g * kv_hs;
@@ -455,9 +460,10 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
   // V: the int8 tile lands key-major in shared memory (16-byte loads and
   // stores); each thread then reads one 4-code word of 8 consecutive keys
   // (a warp reads 32 consecutive words of a key row: no bank conflicts),
-  // transposes the 4 x 8 bytes with byte permutes and writes 8 keys of each
-  // of its 4 channels as fp16.  An int8 code b becomes the fp16 bit pattern
-  // 0x6400 | (b ^ 0x80) = 1024 + b + 128, and subtracting 1152 leaves b.
+  // transposes the 4 x 8 bytes with byte permutes and puts 8 keys of each of
+  // its 4 channels as fp16 into the channel-major shared tile, which then
+  // leaves in whole 256-byte rows.  An int8 code b becomes the fp16 bit
+  // pattern 0x6400 | (b ^ 0x80) = 1024 + b + 128, and subtracting 1152 leaves b.
 #pragma unroll
   for (int rep = 0; rep < 4; ++rep) {
     const int e = threadIdx.x + 256 * rep;  // 1024 chunks of 16 codes
@@ -488,9 +494,15 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
         o[k >> 1] = *reinterpret_cast<const uint32_t *>(&hv);
       }
       const int ch = 4 * wd + c;
-      *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + kg * 8) =
-          make_uint4(o[0], o[1], o[2], o[3]);
+      vt[ch][kg ^ (wd & 15)] = make_uint4(o[0], o[1], o[2], o[3]);
     }
+  }
+  __syncthreads();
+  // rows out: 16 threads write the 256 bytes of one channel's 128 keys
+#pragma unroll
+  for (int rep = 0; rep < 8; ++rep) {
+    const int ch = rep * 16 + (threadIdx.x >> 4), q = threadIdx.x & 15;
+    *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + q * 8) = vt[ch][q ^ ((ch >> 2) & 15)];
   }
   if (threadIdx.x < BN) {
     const int gk = key0 + threadIdx.x;
