@@ -152,6 +152,24 @@ class ClockSampler:
 _ORACLE_INPUTS = {}
 
 
+def kv_cache_on_device(qas, torch, y: dict, dev):
+    """Queries and the int8 KV cache on the device: the cache is written from the
+    workload's fp32 rows by the library's cache writer (outside any timed region)."""
+    q = torch.from_numpy(y["q"].view(np.int16)).view(torch.bfloat16).to(dev)
+    k = torch.from_numpy(y["k_raw"]).to(dev).permute(1, 0, 2)  # token-major view [Nk, Hkv, 128]
+    v = torch.from_numpy(y["v_raw"]).to(dev).permute(1, 0, 2)
+    hkv, nk, d = y["k_raw"].shape
+    kc = torch.empty((hkv, nk, d), dtype=torch.int8, device=dev)
+    vc = torch.empty_like(kc)
+    ks = torch.empty((hkv, nk), dtype=torch.float16, device=dev)
+    vs = torch.empty_like(ks)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    qas.int8kv_cache_write(k, v, kc, ks, vc, vs, 0, status=status)
+    torch.cuda.synchronize(dev)
+    assert status.item() == 0, "device status set by the cache writer"
+    return q, kc, ks, vc, vs
+
+
 def oracle_sample(target_s: float = 12.0):
     """Time the oracle on one head of the workload: its quantisation and the
     attention of a sample of query rows, scaled to the whole workload."""
@@ -397,12 +415,7 @@ def run_ours(args, rank, world):
     kv = {}
     for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
         wk = synth.int8kv_workload(name)
-        y = synth.int8kv_inputs(wk)
-        tq = torch.from_numpy(y["q"].view(np.int16)).view(torch.bfloat16).to(dev)
-        kc = torch.from_numpy(y["k"]).to(dev)
-        vc = torch.from_numpy(y["v"]).to(dev)
-        ks = torch.from_numpy(y["k_scale"]).to(dev)
-        vs = torch.from_numpy(y["v_scale"]).to(dev)
+        tq, kc, ks, vc, vs = kv_cache_on_device(qas, torch, synth.int8kv_inputs(wk), dev)
         o = torch.empty((wk.Nq, wk.Hq, 128), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(L.int8kv_prompt_attn_workspace(wk.Nq, wk.Hq, wk.Hkv, wk.Nk), dtype=torch.uint8, device=dev)
         for _ in range(3):
@@ -542,10 +555,7 @@ def run_case(args):
         flops = 0
     else:
         wk = synth.Int8KVWorkload("profile_case", 12, args.queries, args.seq, args.heads, max(1, args.heads // 4))
-        y = synth.int8kv_inputs(wk)
-        tq = torch.from_numpy(y["q"].view(np.int16)).view(torch.bfloat16).cuda()
-        kc, vc = torch.from_numpy(y["k"]).cuda(), torch.from_numpy(y["v"]).cuda()
-        ks, vs = torch.from_numpy(y["k_scale"]).cuda(), torch.from_numpy(y["v_scale"]).cuda()
+        tq, kc, ks, vc, vs = kv_cache_on_device(qas, torch, synth.int8kv_inputs(wk), torch.device("cuda"))
         run = lambda: qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0)  # noqa: E731
         flops = wk.flops
     for _ in range(args.reps):

@@ -15,14 +15,13 @@ Generator (one definition, counter-based so any slice can be drawn alone):
   ``u = ((z >> 11) + 0.5) * 2**-53`` and returns
   ``sqrt(-2 ln u1) * cos(2 pi u2)`` in fp64.
 * Storage: fp64 -> fp32 (round to nearest even) -> bf16 (round to nearest
-  even) for bf16 tensors; fp64 -> fp32 for values that are quantised into the
-  int8 KV cache.
+  even) for bf16 tensors; fp64 -> fp32 for the K/V rows of the int8 KV cache.
 
-The int8 KV cache of the prompt-attention workloads is written by the cache
+The int8 KV cache of the prompt-attention workloads is written by a cache
 writer upstream of the attention call (Strata PR #2092, "Setup": the engine
-runs ``--kv int8``; the cache holds int8 K/V with per-token scales).  Its
-recipe is part of the workload: per (kv head, token), ``scale =
-fp16_rn(amax / 127)`` and ``code = clamp(rint(x / scale), -127, 127)``.
+runs ``--kv int8``; the cache holds int8 K/V with per-token scales).  This
+module only draws the fp32 rows that go into it: the device side writes the
+cache with the library's own writer, the host side with the oracle's.
 """
 
 from __future__ import annotations
@@ -219,44 +218,23 @@ def outlier_pairs(w: Int8KVWorkload) -> np.ndarray:
     return np.array(sorted(picked), dtype=np.int64)
 
 
-def _cache_quantise(x32: np.ndarray):
-    """Per-token int8 cache recipe: rows of ``x32`` [..., d] -> (codes, fp16 scales)."""
-    amax = np.max(np.abs(x32), axis=-1)
-    scale16 = (amax / np.float32(127.0)).astype(np.float32).astype(np.float16)
-    s32 = scale16.astype(np.float32)
-    safe = np.where(s32 > 0, s32, np.float32(1.0))
-    q = np.rint((x32 / safe[..., None]).astype(np.float32))
-    q = np.where(s32[..., None] > 0, q, 0.0)
-    codes = np.clip(q, -127, 127).astype(np.int8)
-    return codes, scale16
-
-
 def int8kv_inputs(w: Int8KVWorkload, kv_heads: tuple[int, int] | None = None) -> dict:
-    """q bf16 bits [Nq, Hq, d]; K/V int8 [Hkv, Nk, d]; fp16 scales [Hkv, Nk].
+    """q bf16 bits [Nq, Hq, d] and the fp32 K/V rows of the cache, k_raw / v_raw [Hkv, Nk, d].
 
     ``kv_heads=(g0, g1)`` draws only kv heads g0..g1-1 and the query heads that
     read them (q then has shape [Nq, (g1-g0)*Hq/Hkv, d]).
     """
-    d, Nk, Nq, Hq, Hkv = w.d, w.Nk, w.Nq, w.Hq, w.Hkv
+    d, Nq, Hq, Hkv = w.d, w.Nq, w.Hq, w.Hkv
     g0, g1 = (0, Hkv) if kv_heads is None else kv_heads
     grp = Hq // Hkv
-    outl = outlier_pairs(w)
     q = np.empty((Nq, (g1 - g0) * grp, d), dtype=np.uint16)
     qseed = seed_for(w.config, T_Q, w.sub)
     for t in range(Nq):
         base = (t * Hq + g0 * grp) * d
         x = normal_f64(qseed, base, (g1 - g0) * grp * d)
         q[t] = f32_to_bf16_bits(x.astype(np.float32)).reshape((g1 - g0) * grp, d)
-    res = {"q": q}
     raw = int8kv_raw(w, (g0, g1))
-    for key in ("k", "v"):
-        codes = np.empty((g1 - g0, Nk, d), dtype=np.int8)
-        scales = np.empty((g1 - g0, Nk), dtype=np.float16)
-        for j in range(g1 - g0):
-            codes[j], scales[j] = _cache_quantise(raw[key][j])
-        res[key] = codes
-        res[key + "_scale"] = scales
-    return res
+    return {"q": q, "k_raw": raw["k"], "v_raw": raw["v"]}
 
 
 def int8kv_raw(w: Int8KVWorkload, kv_heads: tuple[int, int] | None = None) -> dict:

@@ -1,6 +1,8 @@
 """Parity of int8kv_prompt_attn (CUDA) with the fp64 oracle of the int8
 KV-cache prompt attention: bf16 output within max-abs 2e-3 and rel-L2 1e-3
-of the oracle rounded to bf16."""
+of the oracle rounded to bf16.  Each side reads its own copy of the cache (the
+oracle's quantiser on the host, the library's cache writer on the device),
+checked bit for bit first."""
 
 import numpy as np
 import pytest
@@ -8,27 +10,20 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_output_close, bf16_dev, bf16_to_f64
+from gpu_helpers import assert_output_close, bf16_to_f64
+from kv_helpers import both_caches
 
 pytestmark = pytest.mark.gpu
 
 
-def to_dev(x):
-    q = bf16_dev(x["q"])
-    kc = torch.from_numpy(x["k"]).cuda()
-    vc = torch.from_numpy(x["v"]).cuda()
-    ks = torch.from_numpy(x["k_scale"]).cuda()
-    vs = torch.from_numpy(x["v_scale"]).cuda()
-    return q, kc, ks, vc, vs
-
-
 def run(qas, w, x):
-    q, kc, ks, vc, vs = to_dev(x)
+    """Both caches, then the attention on the device one; returns (oracle inputs, output)."""
+    host, (q, kc, ks, vc, vs) = both_caches(qas, x)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = qas.int8kv_prompt_attn(q, kc, ks, vc, vs, w.q_pos0, status=status)
     torch.cuda.synchronize()
     assert status.item() == 0
-    return out
+    return host, out
 
 
 def oracle_bf16(w, x, rows, heads):
@@ -53,8 +48,7 @@ SMALL = [
 
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_int8kv_matches_oracle_all_rows(cuda_lib, w):
-    x = synth.int8kv_inputs(w)
-    out = run(cuda_lib, w, x)
+    x, out = run(cuda_lib, w, synth.int8kv_inputs(w))
     rows, heads = np.meshgrid(np.arange(w.Nq), np.arange(w.Hq), indexing="ij")
     ref_b, _ = oracle_bf16(w, x, rows.ravel(), heads.ravel())
     got = bf16_to_f64(out).reshape(-1, 128)
@@ -71,8 +65,7 @@ LONG = [
 
 @pytest.mark.parametrize("w", LONG, ids=lambda w: w.name)
 def test_int8kv_long_key_range_sampled(cuda_lib, w):
-    x = synth.int8kv_inputs(w)
-    out = run(cuda_lib, w, x)
+    x, out = run(cuda_lib, w, synth.int8kv_inputs(w))
     rng = np.random.default_rng(5)
     rows = np.concatenate([rng.integers(0, w.Nq, 60), [0, w.Nq - 1]])
     heads = np.concatenate([rng.integers(0, w.Hq, 60), [0, w.Hq - 1]])
@@ -84,8 +77,7 @@ def test_int8kv_long_key_range_sampled(cuda_lib, w):
 @pytest.mark.parametrize("name", ["prompt32k_q1024", "prompt64k_q512_outliers"])
 def test_int8kv_full_size_sampled(cuda_lib, name):
     w = synth.int8kv_workload(name)
-    x = synth.int8kv_inputs(w)
-    out = run(cuda_lib, w, x)
+    x, out = run(cuda_lib, w, synth.int8kv_inputs(w))
     assert torch.isfinite(out.float()).all()
     rng = np.random.default_rng(11)
     rows = np.concatenate([rng.integers(0, w.Nq, 40), [0, w.Nq - 1, 31, 32]])
@@ -102,8 +94,7 @@ def test_int8kv_quarter_million_token_cache_sampled(cuda_lib):
     """64 queries at the end of a 262,144-token cache (2,048 key tiles, the largest
     split-KV factor): sampled rows against the fp64 oracle."""
     w = synth.Int8KVWorkload("kv_256k", 9, 64, 262144, 8, 2, sub=11)
-    x = synth.int8kv_inputs(w)
-    out = run(cuda_lib, w, x)
+    x, out = run(cuda_lib, w, synth.int8kv_inputs(w))
     rows = np.array([0, 5, 31, 32, 63, 63, 17])
     heads = np.array([0, 7, 3, 4, 0, 7, 5])
     ref_b, _ = oracle_bf16(w, x, rows, heads)
@@ -115,8 +106,7 @@ def test_int8kv_strided_queries_and_output(cuda_lib):
     """q read through a [Nq, Hq, 192] buffer's first 128 channels and the output
     written into a [Nq, Hq + 3, 128] buffer give the same bits as contiguous ones."""
     w = synth.Int8KVWorkload("kv_strided", 9, 45, 400, 8, 2, sub=12)
-    x = synth.int8kv_inputs(w)
-    q, kc, ks, vc, vs = to_dev(x)
+    _, (q, kc, ks, vc, vs) = both_caches(cuda_lib, synth.int8kv_inputs(w))
     ref = cuda_lib.int8kv_prompt_attn(q, kc, ks, vc, vs, w.q_pos0)
     wide = torch.zeros((w.Nq, w.Hq, 192), dtype=torch.bfloat16, device="cuda")
     wide[:, :, :128] = q

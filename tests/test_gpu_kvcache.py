@@ -10,6 +10,7 @@ import torch
 import oracle
 import synth
 from gpu_helpers import assert_output_close, bf16_to_f64
+from kv_helpers import oracle_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -88,7 +89,7 @@ def test_cache_write_reports_a_non_finite_scale(cuda_lib):
 
 def test_cache_write_reproduces_the_workload_cache_and_feeds_the_attention(cuda_lib):
     w = synth.int8kv_workload("tiny_kv_q96_k300")
-    x = synth.int8kv_inputs(w)
+    x = oracle_cache(synth.int8kv_inputs(w))
     raw = synth.int8kv_raw(w)
     # new rows arrive token-major [N, Hkv, 128]; write the whole cache in two appends
     k = torch.from_numpy(np.ascontiguousarray(raw["k"].transpose(1, 0, 2))).cuda()
