@@ -1,6 +1,8 @@
-// sage_attention_host: the dense path on host-resident Q, K, V and output,
-// with the host<->device copies and the quantizers overlapped with the
-// attention kernels.
+// The dense path as one call: sage_attention on device buffers (the three
+// entry points in a row, intermediates in the caller's workspace) and
+// sage_attention_host on host-resident Q, K, V and output, with the
+// host<->device copies and the quantizers overlapped with the attention
+// kernels (the rest of this comment).
 //
 // The (batch, head) problems are independent, so the heads are cut into
 // chunks (growing 1, 2, 4, ... up to the chunk size and shrinking again at
