@@ -199,7 +199,10 @@ sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const
  * sage_attn_fwd_ex) in one call on device buffers, for callers that do not
  * keep the codes: the three steps in a row on one stream, their
  * intermediates in the workspace.  The result is bit for bit that of the
- * three entry points called in a row.
+ * three entry points called in a row.  The steps are those of the table
+ * "SageAttention 2.2.0 internals" ("H3 Performance Roadmap", section
+ * "Measured GB10 Baseline": K smoothing, Q/K INT8 quantization, V FP8
+ * quantization, attention forward).
  *   q, k, v, out, strides, sizes, blocks, sm_scale, causal, lse: as in
  *     sage_quantize_qk, sage_quantize_v and sage_attn_fwd_ex.
  *   workspace: device memory of sage_attention_workspace(B, H, Nq, Nk)
