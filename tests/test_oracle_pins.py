@@ -381,6 +381,90 @@ def test_int8kv_scale_exchange_and_group_sharing():
     assert np.array_equal(o2[0], o2[1])
 
 
+def _int8kv_softmax_f64(q_bits, kc, ks, vc, vs, q_pos0, sm_scale):
+    """Test-side restatement of the int8-KV prompt attention ("Strata PR #2092",
+    description and the table "... error against FP64"): for query i of head h,
+    kv head g = h // (Hq // Hkv), visible keys j <= q_pos0 + i,
+    logits sm_scale * ks_j * (q_i . kc_j) in the natural base, softmax weights
+    times the dequantised values vs_j * vc_j.  Vectorised numpy in fp64."""
+    q = bf16f(q_bits)                                      # [Nq, Hq, 128]
+    Nq, Hq, _ = q.shape
+    Hkv, Nk, _ = kc.shape
+    G = Hq // Hkv
+    kd = kc.astype(np.float64)
+    vdeq = vc.astype(np.float64) * vs.astype(np.float64)[..., None]
+    out = np.empty((Nq, Hq, D))
+    for h in range(Hq):
+        g = h // G
+        logits = sm_scale * ks[g].astype(np.float64)[None, :] * (q[:, h] @ kd[g].T)   # [Nq, Nk]
+        visible = np.arange(Nk)[None, :] <= (q_pos0 + np.arange(Nq))[:, None]
+        logits = np.where(visible, logits, -np.inf)
+        e = np.exp(logits - logits.max(axis=1, keepdims=True))
+        out[:, h] = (e @ vdeq[g]) / e.sum(axis=1, keepdims=True)
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv,Nq,Nk", [(3, 3, 7, 301), (8, 2, 5, 190)])
+def test_int8kv_equals_a_numpy_fp64_softmax_at_ordinary_logits(Hq, Hkv, Nq, Nk):
+    # logits of order 1-10 (not the one-hot or uniform limits), a ragged cache
+    # length and a causal window that moves with the query: a wrong logit scale,
+    # exp2 in place of exp, an off-by-one window or a wrong group map all fail
+    rng = np.random.default_rng(Hq * 1000 + Nk)
+    q_pos0 = Nk - Nq - 3
+    q = bf16(rng.normal(0, 2.0, (Nq, Hq, D)))
+    kc = rng.integers(-127, 128, (Hkv, Nk, D)).astype(np.int8)
+    vc = rng.integers(-127, 128, (Hkv, Nk, D)).astype(np.int8)
+    ks = rng.uniform(0.002, 0.03, (Hkv, Nk)).astype(np.float16)
+    vs = rng.uniform(0.005, 0.05, (Hkv, Nk)).astype(np.float16)
+    sm = 1.0 / math.sqrt(128.0)
+    want = _int8kv_softmax_f64(q, kc, ks, vc, vs, q_pos0, sm)
+    logits = sm * ks[0].astype(np.float64) * (bf16f(q)[:, 0] @ kc[0].astype(np.float64).T)
+    assert 1.0 < np.abs(logits).max() < 30.0          # ordinary logits, not a limit case
+    rows, heads = np.meshgrid(np.arange(Nq), np.arange(Hq), indexing="ij")
+    got, _ = oracle.int8kv_rows(q, kc, ks, vc, vs, q_pos0, rows.ravel(), heads.ravel(), nthreads=1)
+    want = want.reshape(-1, D)
+    assert np.abs(got - want).max() <= 1e-12 * max(1.0, np.abs(want).max())
+
+
+def _row_logits_f32(qc_row, sq, kc, sk, bk, C):
+    """s_j = fl(S_j * fl(fl(sq * sk_blk(j)) * C)) rebuilt from codes and scales."""
+    S = kc.astype(np.int64) @ qc_row.astype(np.int64)
+    t = (np.float32(sq) * sk[np.arange(kc.shape[0]) // bk]).astype(np.float32) * np.float32(C)
+    return (S.astype(np.float32) * t.astype(np.float32)).astype(np.float32)
+
+
+def test_dense_denominator_sums_fp32_p_before_the_fp8_conversion():
+    # Reading A8 ("Sage2 SM89 Temporal Pair Experiment", "Candidate": the order
+    # accumulate_d -> RS_32_to_8): the row sum l adds the fp32 p, not the FP8
+    # P/448.  Logits spread over ~25 binades put 448 p into every E4M3 binade,
+    # the subnormals and below, where the two sums differ by percents; the lse
+    # of the row exposes l directly.
+    rng = np.random.default_rng(88)
+    nq, nk, bk = 6, 333, 64
+    qc = rng.integers(-127, 128, (nq, D)).astype(np.int8)
+    kc = rng.integers(-127, 128, (nk, D)).astype(np.int8)
+    sq = rng.uniform(0.5, 1.0, (nq + 63) // 64).astype(np.float32)
+    sk = rng.uniform(0.5, 1.0, (nk + bk - 1) // bk).astype(np.float32) * np.float32(8.0 / 60000.0 / 0.0884)
+    sk = sk.astype(np.float32)
+    vct = np.zeros((D, oracle.nk_pad(nk)), dtype=np.uint8)
+    vct[:, :nk] = oracle.f32_to_e4m3(rng.uniform(-400, 400, (D, nk)).astype(np.float32))
+    sv = np.full(D, 1.0, dtype=np.float32)
+    _, _, _, lse = oracle.sage_attn_rows(qc, sq, 64, kc, sk, bk, vct, sv, nq, nk, with_lse=True)
+    C = np.float32(oracle.SM_SCALE_D128) * np.float32(1.4426950408889634)
+    spread = []
+    for i in range(nq):
+        s = _row_logits_f32(qc[i], sq[i // 64], kc, sk, bk, C).astype(np.float64)
+        M = s.max()
+        want = math.log(2.0) * (M + math.log2(np.exp2(s - M).sum()))
+        assert abs(lse[i] - want) <= 2e-6 * max(1.0, abs(want)), (i, lse[i], want)
+        # the FP8 sum would be far off: the pin separates the two readings
+        p = np.exp2(s - M).astype(np.float32)
+        p8 = oracle.e4m3_value(oracle.f32_to_e4m3((np.float32(448.0) * p).astype(np.float32))) / 448.0
+        spread.append(abs(math.log(p8.sum()) - math.log(p.astype(np.float64).sum())))
+        assert (s.max() - s.min()) > 20.0
+    assert max(spread) > 1e-3
+
+
 # ---------------------------------------------------------------------------
 # fp16 encoder and the per-token int8 KV cache quantiser
 # ("Strata PR #2092": int8 K/V cache with per-token fp16 scales)
@@ -431,6 +515,45 @@ def test_cache_quantise_properties():
     assert np.all(err[live] <= bound[live])
     # a scale that rounds to 0 gives zero codes
     assert sc[8] == 0 and not codes[8].any()
+
+
+def _cache_quantise_numpy(x32):
+    """Independent numpy restatement of the per-token cache recipe: fp32
+    division amax / 127, rounded to fp16; codes rint(fl(x / scale)) (ties to
+    even) clamped to +-127; zero codes where the fp16 scale is 0."""
+    amax = np.max(np.abs(x32), axis=-1)
+    scale16 = (amax / np.float32(127.0)).astype(np.float32).astype(np.float16)
+    s32 = scale16.astype(np.float32)
+    safe = np.where(s32 > 0, s32, np.float32(1.0))
+    quot = (x32 / safe[..., None]).astype(np.float32)
+    codes = np.clip(np.where(s32[..., None] > 0, np.rint(quot), 0.0), -127, 127).astype(np.int8)
+    return codes, scale16.view(np.uint16)
+
+
+def test_cache_quantise_agrees_with_a_numpy_restatement_including_exact_ties():
+    x = _cache_rows(7, 2000, gain=np.float32(0.7))
+    _, s16 = _cache_quantise_numpy(x)
+    s = s16.view(np.float16).astype(np.float32)
+    rng = np.random.default_rng(70)
+    # put quotients exactly on half-integers (k + 1/2) * scale, and one fp32 step
+    # to either side of them, below the row's amax so the scale stays the same
+    amax = np.abs(x).max(axis=1)
+    for r in range(0, 2000, 2):
+        for c in rng.choice(np.arange(128), 12, replace=False):
+            k = int(rng.integers(-126, 126))
+            v = np.float32((k + 0.5) * float(s[r]))
+            if abs(v) >= amax[r] or abs(x[r, c]) == amax[r]:
+                continue
+            x[r, c] = [v, np.nextafter(v, np.float32(np.inf)), np.nextafter(v, np.float32(-np.inf))][c % 3]
+    codes, sc = oracle.cache_quantise(x)
+    c2, s2 = _cache_quantise_numpy(x)
+    assert np.array_equal(sc, s2)
+    assert np.array_equal(codes, c2)
+    # ties really were hit, and some went to the even neighbour below
+    quot = x / s[:, None]
+    ties = np.abs(quot - np.floor(quot) - 0.5) == 0
+    assert ties.sum() > 1000
+    assert np.any(np.abs(codes[ties].astype(np.float32)) < np.abs(quot[ties]))
 
 
 def test_cache_quantise_zero_row_and_power_of_two():
