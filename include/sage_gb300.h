@@ -116,8 +116,11 @@ sage_status sage_quantize_qk(const void *q_bf16, sage_strides qs, const void *k_
  * kernels overlap on the GPU (different streams, or different host threads)
  * race on it and must be serialised by the caller.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Allocates nothing: no cudaMalloc or cudaFree.
+ * (cudaGetSymbolAddress, with that device current), and so does the first
+ * call after the device's context was destroyed and created anew (e.g. by
+ * cudaDeviceReset, which reloads the library's device code); make those
+ * calls before any stream capture.  Allocates nothing: no cudaMalloc or
+ * cudaFree.
  * ---------------------------------------------------------------------- */
 #define SAGE_QK_NOALLOC_SCRATCH_BYTES (8u << 20)
 sage_status sage_quantize_qk_noalloc(const void *q_bf16, sage_strides qs, const void *k_bf16,
@@ -269,19 +272,23 @@ sage_status sage_attn_fwd_scores_dump(const int8_t *q_codes, const float *q_scal
 
 /* ------------------------------------------------------------------------
  * sage_attn_fwd_fault_test - exercises the failure detection of
- * sage_attn_fwd: the same launch, except that the kernel's load warp issues
- * no copies, so the other warps' bounded waits run out after wait_limit_ns.
- * Every CTA then stops its loops, frees its tensor memory and returns; the
- * kernel sets *status_dev to SAGE_ERR_TIMEOUT.  Nothing faults, traps or
- * hangs, and the CUDA context stays usable.  The output is not written.
- * status_dev must not be NULL; wait_limit_ns > 0.  Test hook only.
+ * sage_attn_fwd: the same launch, except that the kernel's load warp stops
+ * early, so the other warps' bounded waits run out after wait_limit_ns.
+ *   mode 1: the load warp issues no copy at all;
+ *   mode 2: it loads the query tiles and the first key tile, then stops, so
+ *           copies and MMAs are issued before the waits give up.
+ * Every CTA then stops its loops, waits for the copies and MMAs it already
+ * issued, frees its tensor memory and returns; the kernel sets *status_dev
+ * to SAGE_ERR_TIMEOUT.  Nothing faults, traps or hangs, and the CUDA context
+ * stays usable.  The output is not written.  status_dev must not be NULL;
+ * wait_limit_ns > 0; mode 1 or 2.  Test hook only.
  * ---------------------------------------------------------------------- */
 sage_status sage_attn_fwd_fault_test(const int8_t *q_codes, const float *q_scales, const int8_t *k_codes,
                                      const float *k_scales, const uint8_t *v_codes, const float *v_scales,
                                      int B, int H, int Nq, int Nk, int d, int q_block, int k_block,
                                      float sm_scale, void *out_bf16, sage_strides os, void *workspace,
                                      size_t workspace_bytes, int32_t *status_dev, uint64_t wait_limit_ns,
-                                     void *stream);
+                                     int mode, void *stream);
 
 /* ------------------------------------------------------------------------
  * int8kv_prompt_attn - causal prompt attention of bf16 queries over an int8

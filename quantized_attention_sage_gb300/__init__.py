@@ -101,7 +101,7 @@ def lib():
                                    vp, Strides, vp, vp, sz, vp, vp]
     L.sage_attn_fwd_fault_test.restype = i32
     L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
-                                           vp, Strides, vp, sz, vp, C.c_uint64, vp]
+                                           vp, Strides, vp, sz, vp, C.c_uint64, i32, vp]
     L.int8kv_cache_write.restype = i32
     L.int8kv_cache_write.argtypes = [vp, vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i64, i32, vp, vp, i64,
                                      vp, vp]
@@ -283,11 +283,13 @@ def sage_attn_fwd_scores_dump(qk: dict, vq: dict, q_block: int = 64, k_block: in
 
 
 def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: int = 64, k_block: int = 64,
-                             stream=None) -> int:
-    """Launch sage_attn_fwd with its load warp silenced, so every bounded wait runs out.
+                             stream=None, mode: int = 1) -> int:
+    """Launch sage_attn_fwd with its load warp stopped early, so the bounded waits run out.
 
-    Returns the device status word after synchronising (SAGE_ERR_TIMEOUT when the
-    failure detection works).  Test hook: the output is not written."""
+    mode 1: no copy is issued; mode 2: the query tiles and the first key tile are
+    loaded (and their Q.K^T issued) before the waits give up.  Returns the device
+    status word after synchronising (SAGE_ERR_TIMEOUT when the failure detection
+    works).  Test hook: the output is not written."""
     torch = _torch()
     _require_codes(torch, qk, vq)
     qc, kc = qk["q_codes"], qk["k_codes"]
@@ -302,7 +304,7 @@ def sage_attn_fwd_fault_test(qk: dict, vq: dict, wait_limit_ns: int, q_block: in
     _check(L.sage_attn_fwd_fault_test(_ptr(qc), _ptr(qk["q_scales"]), _ptr(kc), _ptr(qk["k_scales"]),
                                       _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block,
                                       k_block, 0.0, _ptr(out), _strides4(out), _ptr(ws), nbytes, _ptr(status),
-                                      int(wait_limit_ns), _stream(stream)), "sage_attn_fwd_fault_test")
+                                      int(wait_limit_ns), int(mode), _stream(stream)), "sage_attn_fwd_fault_test")
     torch.cuda.synchronize(dev)
     return int(status.item())
 

@@ -42,6 +42,35 @@ bool encode_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
   return r == CUDA_SUCCESS;
 }
 
+// Driver entry points for the current context's unique id (cuCtxGetId,
+// CUDA 12.0+).  Ids are never reused within a process, so a cache keyed on the
+// id notices when a device's context was destroyed and created again (after
+// cudaDeviceReset, for instance), where a device ordinal would not.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // 0 stands for "unknown"
+}
+
 int current_sm_count() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -49,14 +78,16 @@ int current_sm_count() {
   return n > 0 ? n : 148;
 }
 
-cudaError_t set_smem_attr_once(const void *kernel, int bytes, unsigned long long *done_mask) {
+cudaError_t set_smem_attr_once(const void *kernel, int bytes, CtxOnce *once) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
-  if (bit && (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  const bool slot = dev >= 0 && dev < CtxOnce::kDevices;
+  const unsigned long long ctx = current_context_id();
+  if (slot && ctx != 0 && once->ctx[dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && bit) __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+  // the call above made the device's context current if it was not yet
+  if (e == cudaSuccess && slot) once->ctx[dev].store(current_context_id(), std::memory_order_release);
   return e;
 }
 
@@ -66,7 +97,7 @@ using namespace sg;
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 
 sage_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SAGE_OK : SAGE_ERR_CUDA; }
 
@@ -233,10 +264,10 @@ sage_status sage_attn_fwd_fault_test(const int8_t *q_codes, const float *q_scale
                                      const float *k_scales, const uint8_t *v_codes, const float *v_scales, int B,
                                      int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale,
                                      void *out_bf16, sage_strides os, void *workspace, size_t workspace_bytes,
-                                     int32_t *status_dev, uint64_t wait_limit_ns, void *stream) {
-  if (status_dev == nullptr || wait_limit_ns == 0) return SAGE_ERR_INVALID_ARG;
+                                     int32_t *status_dev, uint64_t wait_limit_ns, int mode, void *stream) {
+  if (status_dev == nullptr || wait_limit_ns == 0 || (mode != 1 && mode != 2)) return SAGE_ERR_INVALID_ARG;
   return attn_fwd_impl(q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, B, H, Nq, Nk, d, q_block, k_block,
-                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, nullptr, stream, 1,
+                       sm_scale, out_bf16, os, workspace, workspace_bytes, status_dev, nullptr, stream, mode,
                        wait_limit_ns);
 }
 

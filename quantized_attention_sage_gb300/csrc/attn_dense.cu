@@ -78,7 +78,7 @@ struct Params {
   int causal;        // query i sees keys j <= i + (Nk - Nq)
   float *lse;        // per-row log-sum-exp [B*H][Nq] (natural base), or null
   uint64_t wait_ns;  // limit of every bounded wait
-  int fault;         // test hook: 1 = the producer issues no loads, so waits run out
+  int fault;         // test hook: 1 = the producer issues no loads; 2 = only Q and the first K tile
   int pairs;         // query-tile pairs per head
   int n_pairs;       // 1-D grid: the first n_pairs CTAs take pairs, the rest single tiles; -1: 2-D grid
 };
@@ -173,9 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop (uniform values); one elected lane issues.
     const bool leader = elect_one();
-    // Test hook (fault == 1): issue nothing, so that the consumers' bounded
-    // waits run out and the kernel reports SAGE_ERR_TIMEOUT with no copy in
-    // flight.
+    // Test hooks: fault == 1 issues nothing; fault == 2 loads Q and the first
+    // K tile and stops.  Either way the consumers' bounded waits run out and
+    // the kernel reports SAGE_ERR_TIMEOUT.
+    int nk = 0, nv = 0;  // K and V tiles issued
+    bool q_issued = false;
     if (p.fault != 1) {
       if (leader) {
         tma_prefetch_desc(&tmQ);
@@ -188,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sQ + kQBytes / 2, &tmQ, &bars->q_full, 64, q0 + t * BM, bh);
         }
       }
+      q_issued = true;
       __syncwarp();
       auto load_k = [&](int j) -> bool {
         const int s = j % NSK;
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(dst + kKBytes / 2, &tmK, &bars->k_full[s], 64, j * BN, bh);
         }
         __syncwarp();
+        ++nk;
         return true;
       };
       auto load_v = [&](int j) -> bool {
@@ -209,15 +213,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + kOffV + s * kVBytes, &tmV, &bars->v_full[s], j * BN, 0, bh);
         }
         __syncwarp();
+        ++nv;
         return true;
       };
       bool ok = load_k(0);
-      for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
+      if (p.fault != 2) {
+        for (int j = 0; ok && j < T; ++j) {
+          if (j + 1 < T) ok = load_k(j + 1);
+          if (ok) ok = load_v(j);
+        }
       }
       if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
     }
+    // Every copy issued here lands in this CTA's shared memory: wait for the
+    // last phase of each barrier it armed before the CTA may exit, also when
+    // the consumers gave up and no longer wait for them.
+    bool drained = !q_issued || mbar_drain(&bars->q_full, 0, p.wait_ns);
+    for (int s = 0; s < NSK; ++s)
+      if (nk > s) drained &= mbar_drain(&bars->k_full[s], ((nk - 1 - s) / NSK) & 1, p.wait_ns);
+    for (int s = 0; s < NSV; ++s)
+      if (nv > s) drained &= mbar_drain(&bars->v_full[s], ((nv - 1 - s) / NSV) & 1, p.wait_ns);
+    if (!drained && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp <= 3) {
     // ------------------------------------------------------------ MMA issuers
     // tcgen05.mma issue blocks for about one MMA's execution time and takes
@@ -241,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dq = sdesc_sw128(smem_u32(smem + kOffQ)) + uint64_t(t) * kQStep;
         const uint64_t dK0 = sdesc_sw128(smem_u32(smem + kOffK));
         ok = mbar_wait(&bars->q_full, 0, abort, p.wait_ns);
+        int last = -1;  // last key tile whose Q.K^T was committed to s_full[t]
         for (int j = 0; ok && j < T; ++j) {
           const int s = j % NSK;
           ok = mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort, p.wait_ns);
@@ -259,11 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&bars->k_empty[s]);
           }
           __syncwarp();
+          last = j;
         }
+        // the MMAs issued here read shared memory and write TMEM: wait for the
+        // last commit (it covers all of them) before the CTA may free either
+        if (last >= 0 && !mbar_drain(&bars->s_full[t], last & 1, p.wait_ns)) ok = false;
       }
     } else {
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + kOffV));
       const uint64_t dP0 = sdesc_sw128(smem_u32(smem + kOffP));
+      int last_j = -1, last_t = 0;  // last P.V committed to pv_done[last_t]
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % NSV;
         ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort, p.wait_ns);
@@ -279,10 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&bars->pv_done[t]);
           }
           __syncwarp();
+          last_j = j;
+          last_t = t;
         }
         if (ok && leader) tc_commit(&bars->v_empty[s]);
         __syncwarp();
       }
+      if (last_j >= 0 && !mbar_drain(&bars->pv_done[last_t], last_j & 1, p.wait_ns)) ok = false;
     }
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   }
@@ -599,7 +624,7 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.wait_ns = a.wait_ns;
   p.fault = a.fault;
 
-  static unsigned long long attr_done = 0;
+  static CtxOnce attr_done;
   e = set_smem_attr_once(reinterpret_cast<const void *>(sage_attn_fwd_kernel), kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(ceil_div(a.Nq, 2 * BM), BH);

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(smem + kOffQ + kQBytes / 2, &tmQ, &bars->q_full, 64, g * p.G, i0);
     }
     __syncwarp();
+    int nk = 0, nv = 0;  // K and V tiles issued
     auto load_k = [&](int j) -> bool {
       const int s = j % NSK;
       if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
@@ -164,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(dst + kKTile / 2, &tmK, &bars->k_full[s], 64, key0, g);
       }
       __syncwarp();
+      ++nk;
       return true;
     };
     auto load_v = [&](int j) -> bool {
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(smem + kOffVs + s * BN * 4, p.vs + row, BN * 4, &bars->v_full[s]);
       }
       __syncwarp();
+      ++nv;
       return true;
     };
     // order of first use: K0, K1, V0, K2, V1, K3, ...
@@ -188,7 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = load_v(j);
       if (ok && j + 2 < T) ok = load_k(j + 2);
     }
-    if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
+    // Every copy issued here lands in this CTA's shared memory: wait for the
+    // last phase of each barrier it armed before the CTA may exit, also when
+    // the consumers gave up and no longer wait for them.
+    bool drained = mbar_drain(&bars->q_full, 0);
+    for (int s = 0; s < NSK; ++s)
+      if (nk > s) drained &= mbar_drain(&bars->k_full[s], ((nk - 1 - s) / NSK) & 1);
+    for (int s = 0; s < NSV; ++s)
+      if (nv > s) drained &= mbar_drain(&bars->v_full[s], ((nv - 1 - s) / NSV) & 1);
+    if ((!ok || !drained) && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (converged warp)
     // Order: QK(0), QK(1), then per tile j: PV(j) (A = P_j from TMEM), QK(j+2)
@@ -196,6 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // QK(j+2) overwrites P_j only after PV(j) has read it).
     const bool leader = elect_one();
     const uint32_t sQ = smem_u32(smem + kOffQ);
+    // the barrier and phase parity of the last commit (it covers every MMA
+    // issued before it)
+    uint64_t *last_bar = nullptr;
+    uint32_t last_par = 0;
     auto issue_qk = [&](int j) -> bool {
       const int s = j % NSK;
       if (!mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort)) return false;
@@ -211,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&bars->k_empty[s]);
       }
       __syncwarp();
+      last_bar = &bars->s_full[j & 1];
+      last_par = (j >> 1) & 1;
       return true;
     };
     bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0) && (T < 2 || issue_qk(1));
@@ -235,8 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(&bars->v_empty[s]);
       }
       __syncwarp();
+      last_bar = &bars->pv_done[j & 1];
+      last_par = (j >> 1) & 1;
       if (j + 2 < T) ok = issue_qk(j + 2);
     }
+    // the MMAs read shared memory and write TMEM: wait for the last commit
+    // before the CTA may free either
+    if (last_bar != nullptr && !mbar_drain(last_bar, last_par)) ok = false;
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / rescale / partials
@@ -655,7 +677,7 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   p.part_o = po;
   p.part_ml = pml;
   p.status = a.status;
-  static unsigned long long attr_done = 0;
+  static CtxOnce attr_done;
   e = set_smem_attr_once(reinterpret_cast<const void *>(int8kv_attn_kernel), kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
   int8kv_attn_kernel<<<dim3(L.nsplit, L.nqt, a.Hkv), kThreads, kSmemBytes, st>>>(tq, tk, tv, p);

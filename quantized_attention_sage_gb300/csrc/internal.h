@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
@@ -19,10 +20,18 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // SM count of the current device (queried per call: a process may drive GPUs
 // of different sizes).
 int current_sm_count();
-// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device):
-// the attribute belongs to the device's context, so a process-wide "done" flag
-// would leave a second device without it.
-cudaError_t set_smem_attr_once(const void *kernel, int bytes, unsigned long long *done_mask);
+// Unique id (+1) of the calling thread's current CUDA context, 0 if none or
+// unknown.  A new context (after cudaDeviceReset, say) gets a new id.
+unsigned long long current_context_id();
+// Per-device record of the context in which a one-time set-up was done.
+struct CtxOnce {
+  static constexpr int kDevices = 64;
+  std::atomic<unsigned long long> ctx[kDevices] = {};
+};
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device
+// context): the attribute belongs to the context, so a process-wide "done"
+// flag would leave a second device, or the device after a reset, without it.
+cudaError_t set_smem_attr_once(const void *kernel, int bytes, CtxOnce *once);
 __host__ __device__ inline int nk_pad(int nk) { return ceil_div(nk, kTile) * kTile; }
 
 // Host-side argument checks shared by the entry points.

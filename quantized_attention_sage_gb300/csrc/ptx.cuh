@@ -98,6 +98,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// Wait for a phase that this CTA's own copies or MMAs will complete (they
+// target valid memory and finish by themselves): bounded by limit_ns but not
+// cut short by an abort flag, so that a CTA that gives up waits for what it
+// already issued before it frees its shared and tensor memory.
+__device__ __forceinline__ bool mbar_drain(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if ((i & 7u) == 0 && globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
 // One lane of the (converged) warp returns true.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;

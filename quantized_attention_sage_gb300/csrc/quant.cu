@@ -325,22 +325,28 @@ static __device__ __align__(256) float g_qk_scratch[kNoAllocScratchBytes / sizeo
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_qk_scratch on the current device, looked up once per
-// device (cudaGetSymbolAddress with that device current).  In host code the
-// array's name is only a host-side stand-in, never a device address.
+// Device address of g_qk_scratch on the current device, looked up with
+// cudaGetSymbolAddress (that device current) once per device context: the
+// first call on a device, and again when the device's context is no longer
+// the one the address was taken in (after cudaDeviceReset the module is
+// loaded anew, possibly elsewhere).  In host code the array's name is only a
+// host-side stand-in, never a device address.
 static cudaError_t noalloc_scratch(float **out) {
   static std::mutex mu;
   static float *ptrs[kMaxDevices] = {};
+  static unsigned long long ctxs[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (ptrs[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  if (ptrs[dev] == nullptr || ctx == 0 || ctx != ctxs[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_qk_scratch);
     if (e != cudaSuccess) return e;
     ptrs[dev] = static_cast<float *>(p);
+    ctxs[dev] = current_context_id();  // the lookup made the context current
   }
   *out = ptrs[dev];
   return cudaSuccess;

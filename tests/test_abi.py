@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_abi_version_and_status_strings(L):
-    assert L.sage_abi_version() == 1
+    assert L.sage_abi_version() == 2
     assert L.sage_status_string(0) == b"ok"
     assert L.sage_status_string(4) == b"workspace too small"
     assert L.sage_status_string(99) == b"unknown status"
@@ -205,3 +205,25 @@ def test_one_call_dense_path_rejects_bad_arguments(L):
     assert call(qs=s4(24 * 256 * 128, 256 * 128, 132)) == 1
     assert call(lse=FAKE + 2) == 1
     assert call(wsb=ws - 1) == 4
+
+
+def test_noalloc_size_check_accepts_exactly_the_limit_and_rejects_one_more(L):
+    """The allocation-free entry point's size check, on the host only: a problem
+    with B*H*ceil(Nk/256) == 16384 K-mean partial rows fills its fixed 8 MiB
+    scratch exactly and passes the check; one more row is SAGE_ERR_TOO_LARGE.
+    Without a GPU the accepted call then stops at the CUDA device query
+    (SAGE_ERR_CUDA) before anything could be launched on the fake pointers, so
+    this test runs only where no CUDA device is visible."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: a visible GPU would run the accepted call")
+    f = L.sage_quantize_qk_noalloc
+    f.restype = C.c_int
+    f.argtypes = [C.c_void_p, Strides, C.c_void_p, Strides] + [C.c_int] * 7 + [C.c_void_p] * 6
+    H, Nk = 64, 256 * 256
+    st = Strides(H * Nk * 128, Nk * 128, 128)
+    at_limit = f(FAKE, st, FAKE, st, 1, H, 64, Nk, 128, 64, 64, FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert at_limit != 6 and at_limit == 3
+    over = f(FAKE, st, FAKE, st, 1, H, 64, Nk + 1, 128, 64, 64, FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert over == 6

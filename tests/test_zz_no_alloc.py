@@ -65,11 +65,32 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls(cuda_lib):
             assert torch.equal(got[key], ref[key]), f"{w.name}: {key}"
 
 
+def test_noalloc_accepts_a_problem_exactly_at_its_scratch_limit(cuda_lib):
+    # B*H*ceil(Nk/256) == 16384 fills the 8 MiB array exactly: accepted, and
+    # equal to the workspace entry point (a one-off in the size check, or in
+    # the partial rows the kernels touch, would show here)
+    B, H, Nq, Nk = 1, 64, 64, 256 * 256
+    gen = torch.Generator(device="cuda").manual_seed(5)
+    q = torch.randn((B, H, Nq, 128), generator=gen, device="cuda").to(torch.bfloat16)
+    k = (torch.randn((B, H, Nk, 128), generator=gen, device="cuda") + 3.0).to(torch.bfloat16)
+    got = call_noalloc(cuda_lib, q, k, 64, 128)
+    ref = cuda_lib.sage_quantize_qk(q, k, 64, 128)
+    torch.cuda.synchronize()
+    for key in ("q_codes", "q_scales", "k_codes", "k_scales", "k_mean"):
+        assert torch.equal(got[key], ref[key]), key
+    del q, k, got, ref
+    torch.cuda.empty_cache()
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch(cuda_lib):
     f = noalloc_fn(cuda_lib)
     fake = 1 << 20  # aligned, never dereferenced: the size check rejects first
     H, Nk = 65, 256 * 253  # 65 * 253 partial rows > 16384
+    assert H * (Nk // 256) > 16384
     st = Strides(H * Nk * 128, Nk * 128, 128)
     code = f(fake, st, fake, st, 1, H, Nk, Nk, 128, 64, 64, fake, fake, fake, fake, fake, None)
     assert code == SAGE_ERR_TOO_LARGE
     assert b"scratch" in cuda_lib.lib().sage_status_string(code)
+    # one more chunk of keys than fits, with a single head
+    code = f(fake, st, fake, st, 1, 1, 8, 256 * 16384 + 1, 128, 64, 64, fake, fake, fake, fake, fake, None)
+    assert code == SAGE_ERR_TOO_LARGE
