@@ -17,9 +17,10 @@ Also measured in the same run (JSON keys, not extra lines):
   * cpu_baseline: the CPU oracle on a bounded sample of the workload.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-Under torchrun every rank runs the full workload on its own GPU (heads of
-independent problems, no collective on the data path: weak scaling); rank 0
-prints the line with the maximum time over ranks.
+Under torchrun the global batch holds one 24-head problem per rank and the
+24 * N independent heads are split over the ranks by the library's
+sage_shard_range (24 heads each, no collective on the data path: weak
+scaling); rank 0 prints the line with the maximum time over ranks.
 """
 
 from __future__ import annotations
@@ -277,7 +278,14 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
 
     w = synth.dense_workload(WORKLOAD)
-    x = synth.dense_inputs(w)
+    # Multi-GPU: the global batch holds one 24-head problem per rank, i.e.
+    # 24 * world independent heads, and sage_shard_range gives each rank its
+    # contiguous share of them (24 heads: weak scaling, no collective on the
+    # data path).  With one rank this is exactly the single-GPU workload.
+    g = synth.DenseWorkload(WORKLOAD, w.config, 1, w.H * world, w.Nq, w.Nk, w.block)
+    h0, h1 = qas.sage_shard_range(g.H, world, rank)
+    assert h1 - h0 == w.H
+    x = synth.dense_inputs(g, heads=(h0, h1))
 
     def to_pinned(bits):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -498,7 +506,8 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded SplitMix64/Box-Muller, the workload's shapes)",
         "config": {"workload": WORKLOAD, "B": 1, "H": 24, "Nq": 37810, "Nk": 37810, "d": 128, "q_block": 128,
                    "k_block": 128, "causal": False, "l2": "inputs larger than L2 (696 MB of Q/K/V)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": (f"heads sharded: {w.H * world} heads over {world} ranks by sage_shard_range, "
+                                   "no collective on the data path" if world > 1 else "single GPU")},
         "roofline": {"kernel": "sage_attn_fwd (int8->fp16 image pass + tcgen05 attention kernel)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_mixed, "unit": "TFLOP/s",
                      "frac": achieved / peak_mixed, "traffic": traffic,

@@ -350,6 +350,25 @@ sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dty
                                int8_t *v_cache, int64_t cache_head_stride, int Ncache, void *k_scale_f16,
                                void *v_scale_f16, int64_t scale_head_stride, int32_t *status_dev, void *stream);
 
+/* ------------------------------------------------------------------------
+ * sage_shard_range - the contiguous range [*begin, *end) of `units`
+ * independent problems that rank `rank` of `world` processes: the first
+ * units % world ranks take ceil(units / world) units, the others
+ * floor(units / world), in rank order (so no rank holds more than
+ * ceil(units / world), and a rank with nothing to do gets begin == end).
+ *
+ * Defines the head partition of a multi-GPU run: every (batch, head)
+ * attention problem is independent, and the Ulysses layout the pages name
+ * for distributed execution ("H3 Performance Roadmap", section "Phase 3:
+ * NVFP4 Fused Projection Prototype", the paragraph on the direct-layout
+ * target: QKV tiles land in rank-destined Ulysses buffers) puts whole heads
+ * on ranks.  Units are the B*H heads of the dense path, the Hkv kv-head
+ * groups of int8kv_prompt_attn, or the tokens of a sequence-sharded tensor.
+ * Host only, no CUDA call.  SAGE_ERR_INVALID_ARG for units < 0, world < 1,
+ * rank outside [0, world) or a NULL output pointer.
+ * ---------------------------------------------------------------------- */
+sage_status sage_shard_range(int64_t units, int world, int rank, int64_t *begin, int64_t *end);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ from .build import LIB, build as _build_lib
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
     "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
-    "sage_attention", "sage_attention_host",
+    "sage_attention", "sage_attention_host", "sage_shard_range",
     "Strides", "STATUS",
 ]
 
@@ -102,6 +102,8 @@ def lib():
     L.sage_attn_fwd_fault_test.restype = i32
     L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                            vp, Strides, vp, sz, vp, C.c_uint64, i32, vp]
+    L.sage_shard_range.restype = i32
+    L.sage_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
     L.int8kv_cache_write.restype = i32
     L.int8kv_cache_write.argtypes = [vp, vp, i32, i64, i64, i32, i32, i32, i32, vp, vp, i64, i32, vp, vp, i64,
                                      vp, vp]
@@ -433,3 +435,12 @@ def int8kv_cache_write(k, v, k_cache, k_scale, v_cache, v_scale, pos0: int, stat
 
 def default_sm_scale() -> float:
     return 1.0 / math.sqrt(D)
+
+
+def sage_shard_range(units: int, world: int, rank: int) -> tuple[int, int]:
+    """[begin, end) of the `units` independent problems (heads, kv-head groups or
+    tokens) that rank `rank` of `world` processes: contiguous, in rank order, the
+    first units % world ranks one more (the C ABI's sage_shard_range)."""
+    b, e = C.c_int64(0), C.c_int64(0)
+    _check(lib().sage_shard_range(int(units), int(world), int(rank), C.byref(b), C.byref(e)), "sage_shard_range")
+    return b.value, e.value

@@ -318,6 +318,17 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
   return from_cuda(launch_int8kv(a, static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_shard_range(int64_t units, int world, int rank, int64_t *begin, int64_t *end) {
+  if (units < 0 || world < 1 || rank < 0 || rank >= world || begin == nullptr || end == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  const int64_t base = units / world, extra = units % world;
+  // ranks below `extra` take base + 1 units, the rest base
+  const int64_t b = int64_t(rank) * base + (rank < extra ? rank : extra);
+  *begin = b;
+  *end = b + base + (rank < extra ? 1 : 0);
+  return SAGE_OK;
+}
+
 sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dtype, int64_t src_tok_stride,
                                int64_t src_head_stride, int N, int Hkv, int d, int pos0, int8_t *k_cache,
                                int8_t *v_cache, int64_t cache_head_stride, int Ncache, void *k_scale_f16,
