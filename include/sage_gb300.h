@@ -351,6 +351,22 @@ sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dty
                                void *v_scale_f16, int64_t scale_head_stride, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_conversion_check - check hook: applies, on the device, the four
+ * number-format conversions the kernels use to every fp32 x[i]:
+ *   e4m3[i] = OCP E4M3 code, round to nearest even, saturating to +-448
+ *             (cvt.rn.satfinite.e4m3x2.f32: the V codes and the FP8 P of
+ *             "Sage2 SM89 Temporal Pair Experiment", section "Candidate");
+ *   i8[i]   = round to nearest even integer, clamped to [-127, 127] (the
+ *             Q/K codes and the int8 cache codes);
+ *   bf16[i] = bf16 bits, round to nearest even (the attention outputs);
+ *   f16[i]  = fp16 bits, round to nearest even (the int8 cache scales).
+ * n even and >= 2; every pointer 16-byte aligned device memory of n
+ * elements.  Enqueued on `stream`; for tests that sweep fp32 bit patterns.
+ * ---------------------------------------------------------------------- */
+sage_status sage_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8_t *i8, uint16_t *bf16,
+                                  uint16_t *f16, void *stream);
+
+/* ------------------------------------------------------------------------
  * sage_shard_range - the contiguous range [*begin, *end) of `units`
  * independent problems that rank `rank` of `world` processes: the first
  * units % world ranks take ceil(units / world) units, the others

@@ -73,6 +73,7 @@ def lib():
         L.orc_f16_value_array.argtypes = [P(C.c_uint16), i64, P(f64)]
         L.orc_f32_to_f16_array.argtypes = [P(f32), i64, P(C.c_uint16)]
         L.orc_cache_quantise_rows.argtypes = [P(f32), i64, P(C.c_int8), P(C.c_uint16)]
+        L.orc_f32_to_i8_array.argtypes = [P(f32), i64, P(C.c_int8)]
         _lib = L
     return _lib
 
@@ -114,6 +115,14 @@ def f32_to_f16(x) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.shape, dtype=np.uint16)
     lib().orc_f32_to_f16_array(_p(x, C.c_float), x.size, _p(out, C.c_uint16))
+    return out
+
+
+def f32_to_i8(x) -> np.ndarray:
+    """fp32 -> int8 code: round half to even, saturated to [-127, 127]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.int8)
+    lib().orc_f32_to_i8_array(_p(x, C.c_float), x.size, _p(out, C.c_int8))
     return out
 
 

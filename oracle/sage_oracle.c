@@ -582,3 +582,10 @@ void orc_f32_to_f16_array(const float *x, int64_t n, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_f16(x[i]);
 }
+
+/* the int8 code of a quantised value: round half to even, saturated to
+   [-127, 127] (the last step of the Q/K and cache quantisers) */
+void orc_f32_to_i8_array(const float *x, int64_t n, int8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = (int8_t)rni_sat127((double)x[i]);
+}

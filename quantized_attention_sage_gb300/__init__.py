@@ -102,6 +102,8 @@ def lib():
     L.sage_attn_fwd_fault_test.restype = i32
     L.sage_attn_fwd_fault_test.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32,
                                            vp, Strides, vp, sz, vp, C.c_uint64, i32, vp]
+    L.sage_conversion_check.restype = i32
+    L.sage_conversion_check.argtypes = [vp, i64, vp, vp, vp, vp, vp]
     L.sage_shard_range.restype = i32
     L.sage_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
     L.int8kv_cache_write.restype = i32
@@ -444,3 +446,17 @@ def sage_shard_range(units: int, world: int, rank: int) -> tuple[int, int]:
     b, e = C.c_int64(0), C.c_int64(0)
     _check(lib().sage_shard_range(int(units), int(world), int(rank), C.byref(b), C.byref(e)), "sage_shard_range")
     return b.value, e.value
+
+
+def sage_conversion_check(x, stream=None) -> dict:
+    """The kernels' four conversions of every fp32 element of the CUDA tensor x
+    (even length): dict(e4m3 uint8, i8 int8, bf16 int16 bits, f16 int16 bits)."""
+    torch = _torch()
+    _require(x, torch.float32, "x", 1)
+    n = x.numel()
+    dev = x.device
+    out = dict(e4m3=torch.empty(n, dtype=torch.uint8, device=dev), i8=torch.empty(n, dtype=torch.int8, device=dev),
+               bf16=torch.empty(n, dtype=torch.int16, device=dev), f16=torch.empty(n, dtype=torch.int16, device=dev))
+    _check(lib().sage_conversion_check(_ptr(x), n, _ptr(out["e4m3"]), _ptr(out["i8"]), _ptr(out["bf16"]),
+                                       _ptr(out["f16"]), _stream(stream)), "sage_conversion_check")
+    return out

@@ -318,6 +318,14 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
   return from_cuda(launch_int8kv(a, static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8_t *i8, uint16_t *bf16,
+                                  uint16_t *f16, void *stream) {
+  if (n < 2 || (n % 2) || !aligned16(x) || !aligned16(e4m3) || !aligned16(i8) || !aligned16(bf16) ||
+      !aligned16(f16))
+    return SAGE_ERR_INVALID_ARG;
+  return from_cuda(launch_conversion_check(x, n, e4m3, i8, bf16, f16, static_cast<cudaStream_t>(stream)));
+}
+
 sage_status sage_shard_range(int64_t units, int world, int rank, int64_t *begin, int64_t *end) {
   if (units < 0 || world < 1 || rank < 0 || rank >= world || begin == nullptr || end == nullptr)
     return SAGE_ERR_INVALID_ARG;

@@ -128,6 +128,20 @@ def test_dense_full_size_videodit_sampled(cuda_lib):
         assert rel64 < 0.1
 
 
+def test_dense_full_size_videodit_whole_head(cuda_lib):
+    """The 37,810-token, 24-head workload in the launch configuration the
+    benchmark times; one whole head (all 37,810 rows and 128 channels, plus
+    its codes, scales and K mean) against the oracle at the full bar."""
+    w = synth.dense_workload("videodit_b1h24n37810")
+    x = synth.dense_inputs(w)
+    q, k, v = bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"])
+    qk, vq, out = run_dense(cuda_lib, q, k, v, w.block, w.block)
+    h = 11
+    (max_abs, rel), _ = check_head(qk, vq, out, 0, h, x["q"][0, h], x["k"][0, h], x["v"][0, h],
+                                   w.block, w.block, tag=f"videodit whole head {h}")
+    print(f"videodit whole head {h}: {w.Nq} rows, vs oracle max-abs {max_abs:.2e} rel-L2 {rel:.2e}")
+
+
 @pytest.mark.parametrize("name", ["tiny_b1h2n256", "sweep_b1h4n1", "sweep_b1h4n129", "sweep_b1h4n257"])
 def test_dense_int32_scores_are_exact(cuda_lib, name):
     """The scores the tensor cores produce (kind::f16 over fp16 images of the

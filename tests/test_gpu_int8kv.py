@@ -90,6 +90,23 @@ def test_int8kv_full_size_sampled(cuda_lib, name):
           f"vs unrounded fp64 max-abs {np.abs(got - ref).max():.2e}")
 
 
+@pytest.mark.parametrize("name", ["prompt32k_q1024", "prompt64k_q512_outliers"])
+def test_int8kv_full_size_whole_kv_group(cuda_lib, name):
+    """Every row of one whole kv-head group (its 4 query heads x all queries)
+    of the full-size chunk against the fp64 oracle at the full bar."""
+    w = synth.int8kv_workload(name)
+    x, out = run(cuda_lib, w, synth.int8kv_inputs(w))
+    G = w.Hq // w.Hkv
+    g = w.Hkv - 1
+    rows, heads = np.meshgrid(np.arange(w.Nq), np.arange(g * G, (g + 1) * G), indexing="ij")
+    rows, heads = rows.ravel(), heads.ravel()
+    ref_b, ref = oracle_bf16(w, x, rows, heads)
+    got = bf16_to_f64(out[torch.as_tensor(rows).cuda(), torch.as_tensor(heads).cuda()])
+    max_abs, rel = assert_output_close(got, ref_b, f"{name} kv group {g}")
+    print(f"{name} kv group {g}: {rows.size} rows, max-abs {max_abs:.2e} rel-L2 {rel:.2e}; "
+          f"vs unrounded fp64 rel-L2 {np.linalg.norm(got - ref) / np.linalg.norm(ref):.2e}")
+
+
 def test_int8kv_quarter_million_token_cache_sampled(cuda_lib):
     """64 queries at the end of a 262,144-token cache (2,048 key tiles, the largest
     split-KV factor): sampled rows against the fp64 oracle."""

@@ -489,6 +489,17 @@ def test_f16_encode_matches_library_rne():
     assert np.array_equal(oracle.f32_to_f16(allx), want)
 
 
+def test_int8_code_rounds_half_to_even_and_saturates():
+    k = np.arange(-140, 141, dtype=np.float64)
+    half = (k + 0.5).astype(np.float32)
+    x = np.concatenate([half, np.nextafter(half, np.float32(np.inf)), np.nextafter(half, np.float32(-np.inf)),
+                        np.array([0.0, -0.0, 1e9, -1e9, 126.5, 127.5, -127.5, 2.0**-30], dtype=np.float32),
+                        np.random.default_rng(4).uniform(-200, 200, 10000).astype(np.float32)])
+    want = np.clip(np.rint(x.astype(np.float64)), -127, 127).astype(np.int8)  # numpy rint: ties to even
+    assert np.array_equal(oracle.f32_to_i8(x), want)
+    assert oracle.f32_to_i8(np.float32([2.5, 3.5, -2.5]))[:3].tolist() == [2, 4, -2]
+
+
 def _cache_rows(seed, n, gain=1.0):
     rng = np.random.default_rng(seed)
     return (rng.standard_normal((n, 128)) * gain).astype(np.float32)
