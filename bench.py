@@ -207,6 +207,171 @@ def oracle_sample(target_s: float = 12.0):
             "seconds": t_quant + t_rows, "est_full_seconds": est_s}
 
 
+def per_clock_peak(probe: dict, sms: int, mhz: float) -> float:
+    """Mixed TFLOP/s peak of the dense attention (equal FLOPs on kind::f16 and
+    kind::f8f6f4) from the probe's MACs per SM per clock at `mhz`."""
+    p16 = 2 * probe["f16_mac_per_clk_sm"] * sms * mhz * 1e6 / 1e12
+    p8 = 2 * probe["f8_mac_per_clk_sm"] * sms * mhz * 1e6 / 1e12
+    return 2.0 / (1.0 / p16 + 1.0 / p8)
+
+
+def _pct(xs):
+    xs = sorted(xs)
+    at = lambda f: xs[int(round(f * (len(xs) - 1)))]  # noqa: E731
+    return {"p10": at(0.1), "p50": at(0.5), "p90": at(0.9)}
+
+
+def _per_call_ms(torch, fn, reps, stream):
+    """CUDA-event time of each of `reps` calls (after 3 warm-up calls)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record(stream)
+    for i in range(reps):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+
+
+def _rel_l2(got, ref):
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def _bits_f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def _fp64_attention(q, k, v, sm_scale, visible=None):
+    """Unquantised softmax(q k^T sm_scale) v in fp64; visible[i] = keys row i sees (causal)."""
+    s = (q @ k.T) * sm_scale
+    if visible is not None:
+        s = np.where(np.arange(k.shape[0])[None, :] < visible[:, None], s, -np.inf)
+    s -= s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    return (p @ v) / p.sum(axis=1, keepdims=True)
+
+
+def per_config_results(qas, torch, dev, pk, peak_mixed, main):
+    """The five configurations: GPU time (p10/p50/p90 of single calls), effective
+    TFLOP/s and roofline fraction, the CPU oracle's time on the host cores, and
+    parity of whole heads (whole kv-head groups) against the oracle, with the
+    distance of the GPU result from unquantised fp64 attention."""
+    import oracle
+
+    stream = torch.cuda.current_stream()
+    sms_scale = 1.0 / math.sqrt(128.0)
+    res = []
+    p16 = pk["bf16_tflops"]
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    # configs 1 and 2: the one-call dense path on small inputs (latency-bound)
+    for w in synth.dense_workloads():
+        if w.config not in (1, 2):
+            continue
+        x = synth.dense_inputs(w)
+        q, k, v = dev_bf16(x["q"]), dev_bf16(x["k"]), dev_bf16(x["v"])
+        out = torch.empty((w.B, w.H, w.Nq, 128), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(qas.lib().sage_attention_workspace(w.B, w.H, w.Nq, w.Nk), dtype=torch.uint8, device=dev)
+        ms = _per_call_ms(torch, lambda: qas.sage_attention(q, k, v, w.block, w.block, out=out, workspace=ws), 30,
+                          stream)
+        got = out.float().cpu().numpy().astype(np.float64)[0]
+        cpu, refs, threads = [], None, 1
+        for _ in range(3):
+            t0 = time.perf_counter()
+            refs = [oracle.sage_head(x["q"][0, h], x["k"][0, h], x["v"][0, h], w.block, w.block) for h in range(w.H)]
+            cpu.append((time.perf_counter() - t0) * 1e3)
+            threads = refs[0]["threads"]
+        ref = np.stack([_bits_f64(r["out_bf16"]) for r in refs])
+        f64 = np.stack([_fp64_attention(_bits_f64(x["q"][0, h]), _bits_f64(x["k"][0, h]), _bits_f64(x["v"][0, h]),
+                                        sms_scale) for h in range(w.H)])
+        t = _pct(ms)
+        res.append({"config": w.config, "workload": w.name, "gpu_ms": t, "call": "sage_attention (one call)",
+                    "tflops": w.flops / (t["p50"] * 1e-3) / 1e12,
+                    "roofline_frac": w.flops / (t["p50"] * 1e-3) / 1e12 / peak_mixed,
+                    "cpu_oracle_ms": statistics.median(cpu), "cpu_cores": threads, "cpu_extrapolated": False,
+                    "parity": {"rows": w.H * w.Nq, "max_abs": float(np.abs(got - ref).max()),
+                               "rel_l2": _rel_l2(got, ref), "rel_l2_vs_fp64_unquantised": _rel_l2(got, f64)}})
+
+    # config 3: timings of the main loop; one whole head against the oracle
+    # (its time, x 24 heads, is the CPU figure)
+    w = synth.dense_workload(WORKLOAD)
+    h = 11
+    x = synth.dense_inputs(w, heads=(h, h + 1))
+    t0 = time.perf_counter()
+    ref = oracle.sage_head(x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], w.block, w.block)
+    t_head = time.perf_counter() - t0
+    got = main["dense_out"]()[0, h].float().cpu().numpy().astype(np.float64)
+    refb = _bits_f64(ref["out_bf16"])
+    rows = np.random.default_rng(9).choice(w.Nq, 1024, replace=False)
+    f64 = _fp64_attention(_bits_f64(x["q"][0, 0][rows]), _bits_f64(x["k"][0, 0]), _bits_f64(x["v"][0, 0]), sms_scale)
+    t = _pct(main["attn_ms"])
+    res.append({"config": w.config, "workload": w.name, "gpu_ms": t, "call": "sage_attn_fwd",
+                "step_ms": _pct(main["step_ms"]), "tflops": w.flops / (t["p50"] * 1e-3) / 1e12,
+                "roofline_frac": w.flops / (t["p50"] * 1e-3) / 1e12 / peak_mixed,
+                "cpu_oracle_ms": t_head * w.H * 1e3, "cpu_cores": ref["threads"], "cpu_extrapolated": True,
+                "cpu_note": f"one whole head (quantisation + all {w.Nq} rows) in {t_head:.1f} s, x {w.H} heads",
+                "parity": {"rows": w.Nq, "head": h, "max_abs": float(np.abs(got - refb).max()),
+                           "rel_l2": _rel_l2(got, refb), "rel_l2_vs_fp64_unquantised": _rel_l2(got[rows], f64),
+                           "fp64_rows": int(rows.size)}})
+
+    # configs 4 and 5: one whole kv-head group against the fp64 oracle (its
+    # time, x Hkv groups, is the CPU figure); distance from fp64 attention over
+    # the unquantised fp32 K/V rows of that group
+    for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
+        wk = synth.int8kv_workload(name)
+        y = synth.int8kv_inputs(wk)
+        tq, kc, ks, vc, vs = kv_cache_on_device(qas, torch, y, dev)
+        o = torch.empty((wk.Nq, wk.Hq, 128), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(qas.lib().int8kv_prompt_attn_workspace(wk.Nq, wk.Hq, wk.Hkv, wk.Nk), dtype=torch.uint8,
+                         device=dev)
+        ms = _per_call_ms(torch, lambda: qas.int8kv_prompt_attn(tq, kc, ks, vc, vs, wk.q_pos0, out=o, workspace=ws),
+                          20, stream)
+        G = wk.Hq // wk.Hkv
+        g = wk.Hkv - 1
+        host = {"q": y["q"]}
+        for key in ("k", "v"):
+            codes, bits = oracle.cache_quantise(y[key + "_raw"])
+            host[key], host[key + "_scale"] = codes, bits.view(np.float16)
+        assert np.array_equal(kc.cpu().numpy(), host["k"]) and np.array_equal(vc.cpu().numpy(), host["v"])
+        rr, hh = np.meshgrid(np.arange(wk.Nq), np.arange(g * G, (g + 1) * G), indexing="ij")
+        rr, hh = rr.ravel(), hh.ravel()
+        t0 = time.perf_counter()
+        ref, threads = oracle.int8kv_rows(host["q"], host["k"], host["k_scale"], host["v"], host["v_scale"],
+                                          wk.q_pos0, rr, hh)
+        t_grp = time.perf_counter() - t0
+        refb = oracle.bf16_value(oracle.f32_to_bf16(ref.astype(np.float32)))
+        got = o[torch.as_tensor(rr).to(dev), torch.as_tensor(hh).to(dev)].float().cpu().numpy().astype(np.float64)
+        f64 = np.concatenate([_fp64_attention(_bits_f64(y["q"][:, hd]), y["k_raw"][g].astype(np.float64),
+                                              y["v_raw"][g].astype(np.float64), sms_scale,
+                                              visible=wk.q_pos0 + np.arange(wk.Nq) + 1)
+                              for hd in range(g * G, (g + 1) * G)])
+        got_by_head = np.concatenate([got[hh == hd] for hd in range(g * G, (g + 1) * G)])
+        t = _pct(ms)
+        visible = 4 * wk.visible_pairs * 128 * wk.Hq
+        res.append({"config": wk.config, "workload": name, "gpu_ms": t, "call": "int8kv_prompt_attn",
+                    "tflops": wk.flops / (t["p50"] * 1e-3) / 1e12,
+                    "tflops_causal": visible / (t["p50"] * 1e-3) / 1e12,
+                    "roofline_frac": visible / (t["p50"] * 1e-3) / 1e12 / p16,
+                    "cpu_oracle_ms": t_grp * wk.Hkv * 1e3, "cpu_cores": threads, "cpu_extrapolated": True,
+                    "cpu_note": f"one whole kv group ({rr.size} rows) in {t_grp:.1f} s, x {wk.Hkv} groups",
+                    "parity": {"rows": int(rr.size), "kv_group": g, "max_abs": float(np.abs(got - refb).max()),
+                               "rel_l2": _rel_l2(got, refb),
+                               "rel_l2_vs_fp64_unquantised": _rel_l2(got_by_head, f64)}})
+        del tq, kc, ks, vc, vs, o, ws
+    return res, {"value": w.flops / (t_head * w.H) / 1e12, "unit": UNIT, "cores": int(ref_threads(res)),
+                 "kind": "oracle", "extrapolated": True,
+                 "sample": (f"head {h} of {WORKLOAD}: quantisation and all {w.Nq} query rows "
+                            f"({t_head:.1f} s), scaled to {w.H} heads")}
+
+
+def ref_threads(res):
+    return next(r["cpu_cores"] for r in res if r["config"] == 3)
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
@@ -352,7 +517,9 @@ def run_ours(args, rank, world):
         "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
         "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
     }
-    attn_ms = sorted(e[2].elapsed_time(e[3]) for e in evs)
+    step_each = [e[0].elapsed_time(e[3]) for e in evs]
+    attn_each = [e[2].elapsed_time(e[3]) for e in evs]
+    attn_ms = sorted(attn_each)
     comp["sage_attn_fwd_ms_p10_p50_p90"] = [attn_ms[int(0.1 * (len(attn_ms) - 1))],
                                             attn_ms[int(0.5 * (len(attn_ms) - 1))],
                                             attn_ms[int(0.9 * (len(attn_ms) - 1))]]
@@ -467,6 +634,15 @@ def run_ours(args, rank, world):
                                   "tokens": wk.Nk, "Hkv": wk.Hkv}
     assert status.item() == 0, "device status set in int8kv_cache_write"
 
+    # ---- per-clock rates of the instructions the dense kernel issues (one CTA per SM)
+    probe = {}
+    for kind, key, iters in ((0, "f16_mac_per_clk_sm", 50000), (1, "f8_mac_per_clk_sm", 50000),
+                             (2, "ex2_per_clk_sm", 1000)):
+        qas.sage_probe_rates(kind, max(1, iters // 10), dev)  # warm-up
+        r = qas.sage_probe_rates(kind, iters, dev)
+        probe[key] = r["per_clock"]
+        probe[key.replace("_per_clk_sm", "_probe_mhz")] = r["mhz"]
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -515,7 +691,13 @@ def run_ours(args, rank, world):
                                    f"fp8/bf16 ratio) for the P.V half"),
                      # the softmax's MUFU demand: one ex2 per score
                      "exp2_per_sm_per_clock": (w.B * w.H * w.Nq * w.Nk) / (comp["sage_attn_fwd_ms"] * 1e-3)
-                     / (current_sms(dev) * 1e6 * ((clocks or {}).get("sm_mhz") or 2070.0))},
+                     / (current_sms(dev) * 1e6 * ((clocks or {}).get("sm_mhz") or 2070.0)),
+                     # the same call against the tensor core's own rates, measured by the
+                     # library's probe (MACs per SM per clock) at the clock sampled in the
+                     # timed region
+                     "peak_per_clock": probe,
+                     "frac_per_clock": achieved / per_clock_peak(probe, current_sms(dev),
+                                                                 (clocks or {}).get("sm_mhz") or 2070.0)},
         "components": comp,
         "quantizers": quantizers,
         "causal_lse": causal,
@@ -525,8 +707,11 @@ def run_ours(args, rank, world):
         "gpu_launches": 9 * args.steps,
     }
     if not args.no_cpu_baseline:
-        cb = oracle_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        configs, cb = per_config_results(qas, torch, dev, pk, peak_mixed,
+                                         {"dense_out": lambda: qas.sage_attn_fwd(qk, vq, bq, bk, workspace=ws_a),
+                                          "attn_ms": attn_each, "step_ms": step_each})
+        line["configs"] = configs
+        line["cpu_baseline"] = cb
         line["cpu_baseline"]["cpu"] = cpu_model()
     print(json.dumps(line), flush=True)
     if dist:

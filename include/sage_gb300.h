@@ -367,6 +367,28 @@ sage_status sage_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8
                                   uint16_t *f16, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_probe_rates - measurement hook for the roofline of the attention
+ * kernels: runs one CTA per SM (grid = the device's SM count), each doing a
+ * fixed amount of one kind of work, and writes the SM clock cycles (clock64)
+ * that CTA took to cycles[cta]:
+ *   kind 0: iters blocks of 128 x 128 x 128 MACs as tcgen05.mma kind::f16
+ *           M128 N128 K16 (8 per block), operands in shared memory, fp32
+ *           accumulators in TMEM: the Q.K^T instruction of the dense path;
+ *   kind 1: the same blocks as kind::f8f6f4 E4M3 M128 N128 K32 (4 per
+ *           block): the P.V instruction of the dense path;
+ *   kind 2: iters x 64 x 8 ex2.approx.f32 on each of 384 threads (MUFU):
+ *           the softmax's exponentials.
+ * MACs (or ex2) per clock per SM = work / cycles; with the call's duration
+ * (CUDA events) cycles also give the SM clock of the run.
+ * cycles: device memory of at least SM-count entries; sink: one device fp32
+ * (never written in practice); status_dev: device int32, SAGE_ERR_TIMEOUT if
+ * the bounded wait for the MMA chain ran out.  kind in 0..2, 1 <= iters <=
+ * 2^20.  Not part of the attention path; called by the benchmark.
+ * ---------------------------------------------------------------------- */
+sage_status sage_probe_rates(int kind, int iters, unsigned long long *cycles, float *sink, int32_t *status_dev,
+                             void *stream);
+
+/* ------------------------------------------------------------------------
  * sage_shard_range - the contiguous range [*begin, *end) of `units`
  * independent problems that rank `rank` of `world` processes: the first
  * units % world ranks take ceil(units / world) units, the others

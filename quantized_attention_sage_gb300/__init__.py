@@ -104,6 +104,8 @@ def lib():
                                            vp, Strides, vp, sz, vp, C.c_uint64, i32, vp]
     L.sage_conversion_check.restype = i32
     L.sage_conversion_check.argtypes = [vp, i64, vp, vp, vp, vp, vp]
+    L.sage_probe_rates.restype = i32
+    L.sage_probe_rates.argtypes = [i32, i32, vp, vp, vp, vp]
     L.sage_shard_range.restype = i32
     L.sage_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
     L.int8kv_cache_write.restype = i32
@@ -460,3 +462,32 @@ def sage_conversion_check(x, stream=None) -> dict:
     _check(lib().sage_conversion_check(_ptr(x), n, _ptr(out["e4m3"]), _ptr(out["i8"]), _ptr(out["bf16"]),
                                        _ptr(out["f16"]), _stream(stream)), "sage_conversion_check")
     return out
+
+
+def sage_probe_rates(kind: int, iters: int, device=None) -> dict:
+    """Per-SM rate of one kind of work (0: tcgen05 kind::f16 M128N128K16 MMAs,
+    1: kind::f8f6f4 M128N128K32, 2: MUFU ex2), one CTA per SM, synchronised.
+
+    Returns dict(per_clock = MACs (or ex2) per SM per clock (median over SMs),
+    ms = the launch's duration, mhz = the SM clock implied by cycles / duration)."""
+    torch = _torch()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.zeros(sms, dtype=torch.int64, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    L = lib()
+    a.record(stream)
+    _check(L.sage_probe_rates(int(kind), int(iters), _ptr(cycles), _ptr(sink), _ptr(status),
+                              _stream(stream)), "sage_probe_rates")
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise SageError(int(status.item()), "sage_probe_rates")
+    cyc = cycles.double().cpu()
+    work = iters * (128 ** 3 if kind in (0, 1) else 64 * 8 * 384)
+    ms = a.elapsed_time(b)
+    med = float(cyc.median())
+    return {"per_clock": work / med, "ms": ms, "mhz": float(cyc.max()) / (ms * 1e3)}

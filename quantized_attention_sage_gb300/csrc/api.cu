@@ -326,6 +326,14 @@ sage_status sage_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8
   return from_cuda(launch_conversion_check(x, n, e4m3, i8, bf16, f16, static_cast<cudaStream_t>(stream)));
 }
 
+sage_status sage_probe_rates(int kind, int iters, unsigned long long *cycles, float *sink, int32_t *status_dev,
+                             void *stream) {
+  if (kind < 0 || kind > 2 || iters < 1 || iters > (1 << 20) || cycles == nullptr || sink == nullptr ||
+      status_dev == nullptr)
+    return SAGE_ERR_INVALID_ARG;
+  return from_cuda(launch_rate_probe(kind, iters, cycles, sink, status_dev, static_cast<cudaStream_t>(stream)));
+}
+
 sage_status sage_shard_range(int64_t units, int world, int rank, int64_t *begin, int64_t *end) {
   if (units < 0 || world < 1 || rank < 0 || rank >= world || begin == nullptr || end == nullptr)
     return SAGE_ERR_INVALID_ARG;

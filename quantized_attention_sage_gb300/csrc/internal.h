@@ -123,6 +123,10 @@ cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st);
 cudaError_t launch_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8_t *i8, uint16_t *bf16,
                                     uint16_t *f16, cudaStream_t st);
 
+// rate probes for the roofline (probe.cu)
+cudaError_t launch_rate_probe(int kind, int iters, unsigned long long *cycles, float *sink, int32_t *status,
+                              cudaStream_t st);
+
 // tensor-map encoding through the driver entry point (api.cu)
 bool encode_tmap_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
