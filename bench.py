@@ -2,13 +2,19 @@
 
 One step = the whole dense path over the 37,810-token, 24-head video-DiT
 self-attention workload (B=1, H=24, Nq=Nk=37,810, d=128, Q/K INT8 per
-128-token blocks, FP8 V): sage_quantize_qk + sage_quantize_v + sage_attn_fwd,
-inputs already resident in HBM.  The metric is effective TFLOP/s
-(4 * Nq * Nk * d * H per step); ms per step is reported beside it.
+128-token blocks, FP8 V): sage_quantize_qkv (K smoothing, Q/K INT8 codes as
+their exact fp16 images, V FP8 codes; three launches) + sage_attn_fwd_f16
+(the attention kernel), inputs already resident in HBM.  The metric is
+effective TFLOP/s (4 * Nq * Nk * d * H per step); ms per step is reported
+beside it.
 
 Also measured in the same run (JSON keys, not extra lines):
-  * per-call times of the three dense entry points (CUDA events around each
-    call inside the timed steps) and the roofline of the attention call;
+  * per-call times of the two calls (CUDA events around each call inside the
+    timed steps), the roofline of the attention kernel against the measured
+    peaks and against the tensor core's own per-clock rates (the library's
+    rate probe), and the same path as three separate entry points;
+  * per-config results for the five workloads (GPU time, CPU oracle time,
+    whole-head parity against the oracle);
   * int8kv_prompt_attn on the 32K x 1024 and 64K x 512 int8 KV-cache chunks;
   * e2e: the same step through the public API with pinned host buffers
     (sage_attention_host: host->device copy of Q, K, V and device->host copy
@@ -309,7 +315,7 @@ def per_config_results(qas, torch, dev, pk, peak_mixed, main):
     rows = np.random.default_rng(9).choice(w.Nq, 1024, replace=False)
     f64 = _fp64_attention(_bits_f64(x["q"][0, 0][rows]), _bits_f64(x["k"][0, 0]), _bits_f64(x["v"][0, 0]), sms_scale)
     t = _pct(main["attn_ms"])
-    res.append({"config": w.config, "workload": w.name, "gpu_ms": t, "call": "sage_attn_fwd",
+    res.append({"config": w.config, "workload": w.name, "gpu_ms": t, "call": "sage_attn_fwd_f16",
                 "step_ms": _pct(main["step_ms"]), "tflops": w.flops / (t["p50"] * 1e-3) / 1e12,
                 "roofline_frac": w.flops / (t["p50"] * 1e-3) / 1e12 / peak_mixed,
                 "cpu_oracle_ms": t_head * w.H * 1e3, "cpu_cores": ref["threads"], "cpu_extrapolated": True,
@@ -472,27 +478,42 @@ def run_ours(args, rank, world):
     ws_qk = torch.empty(L.sage_quantize_qk_workspace(B, H, N), dtype=torch.uint8, device=dev)
     ws_v = torch.empty(L.sage_quantize_v_workspace(B, H, N), dtype=torch.uint8, device=dev)
     ws_a = torch.empty(L.sage_attn_fwd_workspace(B, H, N, N), dtype=torch.uint8, device=dev)
+    ws_p = torch.empty(L.sage_quantize_qkv_workspace(B, H, N), dtype=torch.uint8, device=dev)
+    prep = dict(q_codes=torch.empty((B, H, N, D), dtype=torch.float16, device=dev), q_scales=qk["q_scales"],
+                k_codes=torch.empty((B, H, N, D), dtype=torch.float16, device=dev), k_scales=qk["k_scales"],
+                k_mean=qk["k_mean"], v_codes=vq["v_codes"], v_scales=vq["v_scales"])
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    # One step = the whole dense path: the fused preparation (K smoothing, Q/K
+    # INT8 codes written as their exact fp16 images, V FP8 codes: three
+    # launches) and the attention kernel over the images.
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        qas.sage_quantize_qk(q, k, bq, bk, out=qk, workspace=ws_qk)
+        qas.sage_quantize_qkv(q, k, v, bq, bk, images=True, out=prep, workspace=ws_p)
         if ev is not None:
             ev[1].record(stream)
-        qas.sage_quantize_v(v, out=vq, workspace=ws_v)
+        qas.sage_attn_fwd_f16(prep, bq, bk, out=out, status=status)
         if ev is not None:
             ev[2].record(stream)
+
+    # The same path as its three separate entry points (six quantizer launches,
+    # two image passes inside sage_attn_fwd), timed for comparison.
+    def three_calls(ev):
+        ev[0].record(stream)
+        qas.sage_quantize_qk(q, k, bq, bk, out=qk, workspace=ws_qk)
+        ev[1].record(stream)
+        qas.sage_quantize_v(v, out=vq, workspace=ws_v)
+        ev[2].record(stream)
         qas.sage_attn_fwd(qk, vq, bq, bk, out=out, workspace=ws_a, status=status)
-        if ev is not None:
-            ev[3].record(stream)
+        ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert status.item() == 0, "device status set during warm-up"
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -513,17 +534,29 @@ def run_ours(args, rank, world):
     assert status.item() == 0, "device status set during the timed steps"
     ms_step = ms_total / args.steps
     comp = {
-        "sage_quantize_qk_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-        "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-        "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+        "sage_quantize_qkv_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+        "sage_attn_fwd_f16_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
     }
-    step_each = [e[0].elapsed_time(e[3]) for e in evs]
-    attn_each = [e[2].elapsed_time(e[3]) for e in evs]
+    step_each = [e[0].elapsed_time(e[2]) for e in evs]
+    attn_each = [e[1].elapsed_time(e[2]) for e in evs]
     attn_ms = sorted(attn_each)
-    comp["sage_attn_fwd_ms_p10_p50_p90"] = [attn_ms[int(0.1 * (len(attn_ms) - 1))],
-                                            attn_ms[int(0.5 * (len(attn_ms) - 1))],
-                                            attn_ms[int(0.9 * (len(attn_ms) - 1))]]
+    comp["sage_attn_fwd_f16_ms_p10_p50_p90"] = [attn_ms[int(0.1 * (len(attn_ms) - 1))],
+                                                attn_ms[int(0.5 * (len(attn_ms) - 1))],
+                                                attn_ms[int(0.9 * (len(attn_ms) - 1))]]
     value = whole_job_tflops(w.flops, world, ms_step)
+    # the three separate entry points, for comparison (after the timed steps)
+    ev3 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(5)]
+    three_calls(ev3[0])
+    torch.cuda.synchronize()
+    for e in ev3:
+        three_calls(e)
+    torch.cuda.synchronize()
+    assert status.item() == 0, "device status set by the three entry points"
+    comp["three_entry_points"] = {
+        "sage_quantize_qk_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in ev3),
+        "sage_quantize_v_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in ev3),
+        "sage_attn_fwd_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in ev3),
+        "step_ms": statistics.mean(e[0].elapsed_time(e[3]) for e in ev3)}
 
     # ---- end to end through the public API with pinned host buffers: sage_attention_host
     # copies groups of heads in and out on a copy stream while the previous group runs
@@ -650,17 +683,29 @@ def run_ours(args, rank, world):
 
     pk = peaks()
     kv["cache_write_32k_bf16"]["frac_hbm"] = kv["cache_write_32k_bf16"]["gbs"] / pk["hbm_gbs"]
-    # the quantisers against the measured copy bandwidth: algorithmic bytes are
-    # Q and K read (bf16) + codes written for sage_quantize_qk, V read + codes
-    # written (padded to 128 tokens) for sage_quantize_v
+    # the preparation against the measured copy bandwidth.  The method's own
+    # bytes: Q, K, V read once (bf16), Q/K codes (1 B) and V codes (1 B,
+    # padded to 128 tokens) written.  The fused call moves more: K and V are
+    # read twice (the mean / amax must be known before any code) and the Q/K
+    # codes go out as 2-byte fp16 images, which spares the attention its
+    # conversion passes.
     elems = w.B * w.H * w.Nk * 128
-    qbytes = {"sage_quantize_qk": 2 * elems * 2 + 2 * elems,
-              "sage_quantize_v": elems * 2 + w.B * w.H * 128 * qas.nk_pad(w.Nk)}
-    quantizers = {}
-    for name, nb in qbytes.items():
-        ms_q = comp[name + "_ms"]
-        quantizers[name] = {"ms": ms_q, "bytes": nb, "gbs": nb / (ms_q * 1e-3) / 1e9,
-                            "frac_hbm": nb / (ms_q * 1e-3) / 1e9 / pk["hbm_gbs"]}
+    vcodes = w.B * w.H * 128 * qas.nk_pad(w.Nk)
+    method_bytes = 3 * elems * 2 + 2 * elems + vcodes
+    moved_bytes = 3 * elems * 2 + 2 * elems * 2 + 2 * elems * 2 + vcodes
+    ms_p = comp["sage_quantize_qkv_ms"]
+    three = comp["three_entry_points"]
+    quantizers = {
+        "sage_quantize_qkv": {"ms": ms_p, "method_bytes": method_bytes, "moved_bytes": moved_bytes,
+                              "gbs_method": method_bytes / (ms_p * 1e-3) / 1e9,
+                              "gbs_moved": moved_bytes / (ms_p * 1e-3) / 1e9,
+                              "frac_hbm_method": method_bytes / (ms_p * 1e-3) / 1e9 / pk["hbm_gbs"],
+                              "frac_hbm_moved": moved_bytes / (ms_p * 1e-3) / 1e9 / pk["hbm_gbs"],
+                              "launches": 3},
+        "separate": {"sage_quantize_qk_ms": three["sage_quantize_qk_ms"],
+                     "sage_quantize_v_ms": three["sage_quantize_v_ms"],
+                     "image_passes_ms": three["sage_attn_fwd_ms"] - comp["sage_attn_fwd_f16_ms"],
+                     "total_ms": three["step_ms"] - comp["sage_attn_fwd_f16_ms"], "launches": 8}}
     p16 = pk["bf16_tflops"]
     for name in ("prompt32k_q1024", "prompt64k_q512_outliers"):
         # Q.K^T and P.V both on the bf16/f16 tensor path; the fp16 hi/lo split of
@@ -672,7 +717,7 @@ def run_ours(args, rank, world):
     # Q.K^T on the f16 tensor path, P.V on FP8 (2x the f16 rate, nominal ratio):
     # equal FLOPs on both, so the effective peak is the harmonic combination.
     peak_mixed = 2.0 / (1.0 / p16 + 1.0 / (2.0 * p16))
-    achieved = w.flops / (comp["sage_attn_fwd_ms"] * 1e-3) / 1e12
+    achieved = w.flops / (comp["sage_attn_fwd_f16_ms"] * 1e-3) / 1e12
     sha = kernel_sha("attn_dense.cu")[:16]
     traffic = TRAFFIC["bytes"] if TRAFFIC["sha256_prefix"] == sha else None
     line = {
@@ -684,13 +729,13 @@ def run_ours(args, rank, world):
                    "k_block": 128, "causal": False, "l2": "inputs larger than L2 (696 MB of Q/K/V)",
                    "parallelism": (f"heads sharded: {w.H * world} heads over {world} ranks by sage_shard_range, "
                                    "no collective on the data path" if world > 1 else "single GPU")},
-        "roofline": {"kernel": "sage_attn_fwd (int8->fp16 image pass + tcgen05 attention kernel)",
+        "roofline": {"kernel": "sage_attn_fwd_kernel (tcgen05 attention over the fp16 images, sage_attn_fwd_f16)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_mixed, "unit": "TFLOP/s",
                      "frac": achieved / peak_mixed, "traffic": traffic,
                      "peak_note": (f"{pk['source']}: bf16 burst {p16} TFLOP/s for the Q.K^T half, x2 (nominal "
                                    f"fp8/bf16 ratio) for the P.V half"),
                      # the softmax's MUFU demand: one ex2 per score
-                     "exp2_per_sm_per_clock": (w.B * w.H * w.Nq * w.Nk) / (comp["sage_attn_fwd_ms"] * 1e-3)
+                     "exp2_per_sm_per_clock": (w.B * w.H * w.Nq * w.Nk) / (comp["sage_attn_fwd_f16_ms"] * 1e-3)
                      / (current_sms(dev) * 1e6 * ((clocks or {}).get("sm_mhz") or 2070.0)),
                      # the same call against the tensor core's own rates, measured by the
                      # library's probe (MACs per SM per clock) at the clock sampled in the
@@ -704,7 +749,7 @@ def run_ours(args, rank, world):
         "int8kv": kv,
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 9 * args.steps,
+        "gpu_launches": 4 * args.steps,
     }
     if not args.no_cpu_baseline:
         configs, cb = per_config_results(qas, torch, dev, pk, peak_mixed,

@@ -129,6 +129,37 @@ sage_status sage_quantize_qk_noalloc(const void *q_bf16, sage_strides qs, const 
                                      float *k_scales, float *k_mean, void *stream);
 
 /* ------------------------------------------------------------------------
+ * sage_quantize_qkv - the whole preparation of the dense path (what
+ * sage_quantize_qk and sage_quantize_v compute) in three launches for all
+ * heads: one reduction pass over K and V (K chunk sums, V channel maxima),
+ * one finalisation (K mean, V scales), one encoding pass over Q, K and V.
+ *
+ * Defines: the same steps as sage_quantize_qk and sage_quantize_v ("H3
+ * Performance Roadmap", table "SageAttention 2.2.0 internals"), fused as
+ * "Phase 4: Dense Sage-Compatible Attention", item 4 asks (fuse the Q/K/V
+ * preparation where profitable).
+ *
+ * Codes, scales, the K mean and the V codes are bit for bit those of the two
+ * separate entry points.  qk_format selects how the Q/K codes are stored:
+ *   SAGE_QK_INT8: int8 [B,H,N,128] (as sage_quantize_qk);
+ *   SAGE_QK_F16:  the codes' exact fp16 images [B,H,N,128] (every code is
+ *                 an integer of magnitude <= 127), the operand layout the
+ *                 attention's tensor cores read: sage_attn_fwd_f16 takes
+ *                 them with no conversion pass.
+ * q_out, k_out: contiguous, int8 or fp16 as selected; q_scales, k_scales,
+ * k_mean, v_codes, v_scales as in sage_quantize_qk / sage_quantize_v.
+ * Workspace: at least sage_quantize_qkv_workspace(B, H, Nk) bytes.
+ * ---------------------------------------------------------------------- */
+#define SAGE_QK_INT8 0
+#define SAGE_QK_F16 1
+size_t sage_quantize_qkv_workspace(int B, int H, int Nk);
+sage_status sage_quantize_qkv(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                              const void *v_bf16, sage_strides vs, int B, int H, int Nq, int Nk, int d, int q_block,
+                              int k_block, int qk_format, void *q_out, float *q_scales, void *k_out, float *k_scales,
+                              float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * sage_quantize_v - FP8 E4M3 per-channel quantisation of V, written
  * transposed for the P.V product.
  *
@@ -196,6 +227,21 @@ sage_status sage_attn_fwd_ex(const int8_t *q_codes, const float *q_scales, const
                              int B, int H, int Nq, int Nk, int d, int q_block, int k_block, float sm_scale,
                              int causal, void *out_bf16, sage_strides os, float *lse, void *workspace,
                              size_t workspace_bytes, int32_t *status_dev, void *stream);
+
+/* ------------------------------------------------------------------------
+ * sage_attn_fwd_f16 - sage_attn_fwd_ex over the exact fp16 images of the
+ * Q/K codes (as sage_quantize_qkv writes them with SAGE_QK_F16) instead of
+ * the int8 codes: the same attention kernel and result, without the two
+ * conversion passes and without a workspace.  Page and computation as
+ * sage_attn_fwd ("Sage2 SM89 Temporal Pair Experiment", section
+ * "Candidate").
+ *   q_f16 [B,H,Nq,128], k_f16 [B,H,Nk,128]: contiguous fp16 images, 16-byte
+ *   aligned; everything else as sage_attn_fwd_ex.
+ * ---------------------------------------------------------------------- */
+sage_status sage_attn_fwd_f16(const void *q_f16, const float *q_scales, const void *k_f16, const float *k_scales,
+                              const uint8_t *v_codes, const float *v_scales, int B, int H, int Nq, int Nk, int d,
+                              int q_block, int k_block, float sm_scale, int causal, void *out_bf16, sage_strides os,
+                              float *lse, int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
  * sage_attention - the dense path (sage_quantize_qk, sage_quantize_v,

@@ -25,7 +25,7 @@ from .build import LIB, build as _build_lib
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
     "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
-    "sage_attention", "sage_attention_host", "sage_shard_range",
+    "sage_attention", "sage_attention_host", "sage_shard_range", "sage_quantize_qkv", "sage_attn_fwd_f16",
     "Strides", "STATUS",
 ]
 
@@ -106,6 +106,14 @@ def lib():
     L.sage_conversion_check.argtypes = [vp, i64, vp, vp, vp, vp, vp]
     L.sage_probe_rates.restype = i32
     L.sage_probe_rates.argtypes = [i32, i32, vp, vp, vp, vp]
+    L.sage_quantize_qkv_workspace.restype = sz
+    L.sage_quantize_qkv_workspace.argtypes = [i32, i32, i32]
+    L.sage_quantize_qkv.restype = i32
+    L.sage_quantize_qkv.argtypes = [vp, Strides, vp, Strides, vp, Strides, i32, i32, i32, i32, i32, i32, i32, i32,
+                                    vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.sage_attn_fwd_f16.restype = i32
+    L.sage_attn_fwd_f16.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, Strides,
+                                    vp, vp, vp]
     L.sage_shard_range.restype = i32
     L.sage_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
     L.int8kv_cache_write.restype = i32
@@ -261,6 +269,67 @@ def sage_attn_fwd(qk: dict, vq: dict, q_block: int = 64, k_block: int = 64, sm_s
                               _ptr(vq["v_codes"]), _ptr(vq["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
                               float(sm_scale), int(bool(causal)), _ptr(out), _strides4(out), _ptr(lse), _ptr(ws),
                               nbytes, _ptr(status), _stream(stream)), "sage_attn_fwd_ex")
+    return (out, lse) if return_lse else out
+
+
+SAGE_QK_INT8, SAGE_QK_F16 = 0, 1
+
+
+def sage_quantize_qkv(q, k, v, q_block: int = 64, k_block: int = 64, images: bool = True, out=None,
+                      workspace=None, stream=None):
+    """The whole preparation (K smoothing, Q/K INT8 codes, V FP8 codes) in three launches.
+
+    q: [B,H,Nq,128], k, v: [B,H,Nk,128] bf16 CUDA tensors.  Returns dict(q_codes, q_scales,
+    k_codes, k_scales, k_mean, v_codes, v_scales); with ``images`` the Q/K codes are their exact
+    fp16 images (what sage_attn_fwd_f16 reads), otherwise int8 as sage_quantize_qk writes them."""
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, torch.bfloat16, name, 4)
+    if (q.shape[:2] != k.shape[:2] or k.shape != v.shape or q.shape[3] != D or k.shape[3] != D
+            or not (q.device == k.device == v.device)):
+        raise ValueError("q [B,H,Nq,128], k and v [B,H,Nk,128] on one device")
+    B, H, Nq, _ = q.shape
+    Nk = k.shape[2]
+    dev = q.device
+    cd = torch.float16 if images else torch.int8
+    if out is None:
+        out = dict(q_codes=torch.empty((B, H, Nq, D), dtype=cd, device=dev),
+                   q_scales=torch.empty((B, H, -(-Nq // q_block)), dtype=torch.float32, device=dev),
+                   k_codes=torch.empty((B, H, Nk, D), dtype=cd, device=dev),
+                   k_scales=torch.empty((B, H, -(-Nk // k_block)), dtype=torch.float32, device=dev),
+                   k_mean=torch.empty((B, H, D), dtype=torch.float32, device=dev),
+                   v_codes=torch.empty((B, H, D, nk_pad(Nk)), dtype=torch.uint8, device=dev),
+                   v_scales=torch.empty((B, H, D), dtype=torch.float32, device=dev))
+    L = lib()
+    nbytes = L.sage_quantize_qkv_workspace(B, H, Nk)
+    ws = _workspace(nbytes, dev, workspace)
+    _check(L.sage_quantize_qkv(_ptr(q), _strides4(q), _ptr(k), _strides4(k), _ptr(v), _strides4(v), B, H, Nq, Nk, D,
+                               q_block, k_block, SAGE_QK_F16 if images else SAGE_QK_INT8, _ptr(out["q_codes"]),
+                               _ptr(out["q_scales"]), _ptr(out["k_codes"]), _ptr(out["k_scales"]),
+                               _ptr(out["k_mean"]), _ptr(out["v_codes"]), _ptr(out["v_scales"]), _ptr(ws), nbytes,
+                               _stream(stream)), "sage_quantize_qkv")
+    return out
+
+
+def sage_attn_fwd_f16(prep: dict, q_block: int = 64, k_block: int = 64, sm_scale: float = 0.0, out=None,
+                      status=None, stream=None, causal: bool = False, return_lse: bool = False):
+    """The attention over sage_quantize_qkv(..., images=True)'s outputs (fp16 images of the
+    Q/K codes); bf16 [B,H,Nq,128], or (out, lse) with ``return_lse``.  No workspace."""
+    torch = _torch()
+    _require(prep["q_codes"], torch.float16, "q images", 4)
+    _require(prep["k_codes"], torch.float16, "k images", 4)
+    _require(prep["v_codes"], torch.uint8, "v_codes", 4)
+    qi, ki = prep["q_codes"], prep["k_codes"]
+    B, H, Nq, _ = qi.shape
+    Nk = ki.shape[2]
+    dev = qi.device
+    if out is None:
+        out = torch.empty((B, H, Nq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev) if return_lse else None
+    _check(lib().sage_attn_fwd_f16(_ptr(qi), _ptr(prep["q_scales"]), _ptr(ki), _ptr(prep["k_scales"]),
+                                   _ptr(prep["v_codes"]), _ptr(prep["v_scales"]), B, H, Nq, Nk, D, q_block, k_block,
+                                   float(sm_scale), int(bool(causal)), _ptr(out), _strides4(out), _ptr(lse),
+                                   _ptr(status), _stream(stream)), "sage_attn_fwd_f16")
     return (out, lse) if return_lse else out
 
 

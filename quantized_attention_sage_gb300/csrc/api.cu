@@ -160,6 +160,51 @@ sage_status sage_quantize_qk_noalloc(const void *q_bf16, sage_strides qs, const 
                                               static_cast<cudaStream_t>(stream)));
 }
 
+size_t sage_quantize_qkv_workspace(int B, int H, int Nk) {
+  if (B < 1 || H < 1 || Nk < 1) return 0;
+  return prepare_workspace_bytes(B, H, Nk);
+}
+
+sage_status sage_quantize_qkv(const void *q_bf16, sage_strides qs, const void *k_bf16, sage_strides ks,
+                              const void *v_bf16, sage_strides vs, int B, int H, int Nq, int Nk, int d, int q_block,
+                              int k_block, int qk_format, void *q_out, float *q_scales, void *k_out, float *k_scales,
+                              float *k_mean, uint8_t *v_codes, float *v_scales, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (qk_format != SAGE_QK_INT8 && qk_format != SAGE_QK_F16) return SAGE_ERR_INVALID_ARG;
+  if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q_bf16) || !aligned16(k_bf16) || !aligned16(v_bf16) || !aligned16(q_out) || !aligned16(k_out) ||
+      !aligned16(k_mean) || !aligned16(v_codes) || !aligned16(v_scales) || q_scales == nullptr ||
+      k_scales == nullptr || !aligned16(workspace))
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(qs) || !strides_ok(ks) || !strides_ok(vs)) return SAGE_ERR_INVALID_ARG;
+  if (workspace_bytes < sage_quantize_qkv_workspace(B, H, Nk)) return SAGE_ERR_WORKSPACE;
+  PrepArgs a;
+  a.q = q_bf16;
+  a.k = k_bf16;
+  a.v = v_bf16;
+  a.qs = qs;
+  a.ks = ks;
+  a.vs = vs;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.q_block = q_block;
+  a.k_block = k_block;
+  a.images = qk_format == SAGE_QK_F16;
+  a.q_out = q_out;
+  a.k_out = k_out;
+  a.q_scales = q_scales;
+  a.k_scales = k_scales;
+  a.k_mean = k_mean;
+  a.v_codes = v_codes;
+  a.v_scales = v_scales;
+  a.workspace = static_cast<float *>(workspace);
+  return from_cuda(launch_prepare(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t sage_quantize_v_workspace(int B, int H, int Nk) {
   if (B < 1 || H < 1 || Nk < 1) return 0;
   return (size_t(B) * H * ceil_div(Nk, kMeanChunk) * kD + size_t(B) * H * kD) * sizeof(float) + 16;
@@ -226,6 +271,45 @@ static sage_status attn_fwd_impl(const int8_t *q_codes, const float *q_scales, c
   a.wait_ns = wait_ns;
   a.causal = causal;
   a.lse = lse;
+  return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
+}
+
+sage_status sage_attn_fwd_f16(const void *q_f16, const float *q_scales, const void *k_f16, const float *k_scales,
+                              const uint8_t *v_codes, const float *v_scales, int B, int H, int Nq, int Nk, int d,
+                              int q_block, int k_block, float sm_scale, int causal, void *out_bf16, sage_strides os,
+                              float *lse, int32_t *status_dev, void *stream) {
+  if (d != kD) return SAGE_ERR_UNSUPPORTED;
+  if (causal != 0 && causal != 1) return SAGE_ERR_INVALID_ARG;
+  if (causal && Nq > Nk) return SAGE_ERR_UNSUPPORTED;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SAGE_ERR_INVALID_ARG;
+  if ((q_block != 64 && q_block != 128) || (k_block != 64 && k_block != 128)) return SAGE_ERR_UNSUPPORTED;
+  if (!sizes_ok(B, H, Nq) || !sizes_ok(B, H, Nk)) return SAGE_ERR_INVALID_ARG;
+  if (!aligned16(q_f16) || !aligned16(k_f16) || !aligned16(v_codes) || q_scales == nullptr || k_scales == nullptr ||
+      v_scales == nullptr || !aligned16(out_bf16))
+    return SAGE_ERR_INVALID_ARG;
+  if (!strides_ok(os)) return SAGE_ERR_INVALID_ARG;
+  DenseArgs a;
+  a.q_codes = nullptr;
+  a.q_scales = q_scales;
+  a.k_codes = nullptr;
+  a.k_scales = k_scales;
+  a.v_codes = v_codes;
+  a.v_scales = v_scales;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.q_block = q_block;
+  a.k_block = k_block;
+  a.sm_scale = default_scale(sm_scale);
+  a.out = out_bf16;
+  a.os = os;
+  a.q_img = const_cast<void *>(q_f16);
+  a.k_img = const_cast<void *>(k_f16);
+  a.status = status_dev;
+  a.causal = causal;
+  a.lse = lse;
+  a.images_ready = true;
   return from_cuda(launch_attn_dense(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -62,6 +62,21 @@ cudaError_t launch_quantize_qk_noalloc(const void *q, sage_strides qs, const voi
 cudaError_t launch_quantize_v(const void *v, sage_strides vs, int B, int H, int Nk, uint8_t *v_codes,
                               float *v_scales, float *partial, float *inv, cudaStream_t st);
 
+// the whole preparation in three launches (prepare.cu)
+struct PrepArgs {
+  const void *q, *k, *v;  // bf16 [B, H, N, 128] with element strides
+  sage_strides qs, ks, vs;
+  int B, H, Nq, Nk, q_block, k_block;
+  bool images;            // Q/K out as exact fp16 images (else int8 codes)
+  void *q_out, *k_out;    // [B, H, N, 128] int8 or fp16, contiguous
+  float *q_scales, *k_scales, *k_mean;
+  uint8_t *v_codes;       // [B, H, 128, Nk_pad]
+  float *v_scales;
+  float *workspace;       // prepare_workspace_bytes(B, H, Nk)
+};
+size_t prepare_workspace_bytes(int B, int H, int Nk);
+cudaError_t launch_prepare(const PrepArgs &a, cudaStream_t st);
+
 // dense attention (attn_dense.cu)
 struct DenseArgs {
   const int8_t *q_codes;

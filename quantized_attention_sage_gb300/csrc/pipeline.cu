@@ -1,16 +1,18 @@
-// The dense path as one call: sage_attention on device buffers (the three
-// entry points in a row, intermediates in the caller's workspace) and
+// The dense path as one call: sage_attention on device buffers (the fused
+// preparation, sage_quantize_qkv with fp16 images of the Q/K codes, then the
+// attention kernel, intermediates in the caller's workspace) and
 // sage_attention_host on host-resident Q, K, V and output, with the
-// host<->device copies and the quantizers overlapped with the attention
+// host<->device copies and the preparation overlapped with the attention
 // kernels (the rest of this comment).
 //
 // The (batch, head) problems are independent, so the heads are cut into
 // chunks (growing 1, 2, 4, ... up to the chunk size and shrinking again at
 // the end, so that the first copy in and the last copy out are short).  Two
 // streams share the work:
-//   staging stream (the caller's copy stream): host->device copies, the two
-//            quantizers and the fp16 images of the Q/K codes, device->host
-//            copies;
+//   staging stream (the caller's copy stream): host->device copies, the
+//            preparation (three launches: reduction, finalisation, encoding
+//            into fp16 images of the Q/K codes and E4M3 V codes),
+//            device->host copies;
 //   compute stream: the attention kernel of one chunk after another.
 // While the compute stream attends chunk c, the staging stream copies chunk
 // c+2 in, then (once chunk c is done) copies its output out and quantizes
@@ -21,14 +23,14 @@
 // the call (timing disabled) and released as soon as they are enqueued.
 //
 // Per chunk c (slot s = c % 2), in stream order:
-//   staging: H2D q, k, v -> in[s]; quantize in[s] -> codes[s], images[s];
+//   staging: H2D q, k, v -> in[s]; prepare in[s] -> images[s], codes[s];
 //            record q_ready[c]
-//   compute: wait q_ready[c]; attention kernel on codes[s], images[s] -> out[s];
+//   compute: wait q_ready[c]; attention kernel on images[s], codes[s] -> out[s];
 //            record done[c]
-//   staging: wait done[c]; D2H out[s]; quantize chunk c+2 into codes[s], images[s]
+//   staging: wait done[c]; D2H out[s]; prepare chunk c+2 into images[s], codes[s]
 // H2D of chunk c+2 is queued before the wait for done[c]: in[s] was last read
-// by the quantizers of chunk c, earlier on the same stream.  The quantizers
-// of chunk c+2 follow done[c] (codes[s] has been read) and D2H of chunk c
+// by the preparation of chunk c, earlier on the same stream.  The preparation
+// of chunk c+2 follows done[c] (images[s] have been read) and D2H of chunk c
 // (out[s] is drained before attention(c+2), which waits for q_ready[c+2]).
 // The staging stream first waits for the work already queued on the compute
 // stream; at the end the compute stream waits for the last D2H, so the caller
@@ -49,9 +51,9 @@ struct HostLayout {
   int hc;                               // heads per chunk
   size_t q_bytes, k_bytes, o_bytes;     // bf16 chunk buffers
   size_t off_in[2][3], off_out[2];      // inputs (q, k, v) and output per slot
-  size_t off_qc[2], off_kc[2], off_qs[2], off_ks[2], off_mu[2], off_vc[2], off_vs[2], off_wqk[2], off_wv[2];
+  size_t off_qs[2], off_ks[2], off_mu[2], off_vc[2], off_vs[2], off_wp[2];
   size_t off_qi[2], off_ki[2];          // fp16 images of the Q and K codes the attention reads
-  size_t wqk, wv, total;
+  size_t wp, total;
 };
 
 HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
@@ -62,8 +64,7 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
   L.q_bytes = hc * Nq * sg::kD * 2;
   L.k_bytes = hc * Nk * sg::kD * 2;
   L.o_bytes = L.q_bytes;
-  L.wqk = sage_quantize_qk_workspace(1, L.hc, Nk);
-  L.wv = sage_quantize_v_workspace(1, L.hc, Nk);
+  L.wp = sage_quantize_qkv_workspace(1, L.hc, Nk);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -75,15 +76,12 @@ HostLayout host_layout(int B, int H, int Nq, int Nk, int head_chunk) {
     L.off_in[s][1] = take(L.k_bytes);
     L.off_in[s][2] = take(L.k_bytes);
     L.off_out[s] = take(L.o_bytes);
-    L.off_qc[s] = take(hc * Nq * sg::kD);
-    L.off_kc[s] = take(hc * Nk * sg::kD);
     L.off_qs[s] = take(hc * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
     L.off_ks[s] = take(hc * sg::ceil_div(Nk, 64) * sizeof(float));
     L.off_mu[s] = take(hc * sg::kD * sizeof(float));
     L.off_vc[s] = take(hc * sg::kD * size_t(sg::nk_pad(Nk)));
     L.off_vs[s] = take(hc * sg::kD * sizeof(float));
-    L.off_wqk[s] = take(L.wqk);
-    L.off_wv[s] = take(L.wv);
+    L.off_wp[s] = take(L.wp);
     L.off_qi[s] = take(hc * Nq * sg::kD * 2);
     L.off_ki[s] = take(hc * Nk * sg::kD * 2);
   }
@@ -120,11 +118,11 @@ std::vector<int> chunk_starts(int BH, int hc) {
   return first;
 }
 
-// sage_attention: the same three steps on device buffers in one call.  The
-// intermediates of all heads live in the caller's workspace.
+// sage_attention: the preparation and the attention on device buffers in one
+// call.  The intermediates of all heads live in the caller's workspace.
 struct DeviceLayout {
-  size_t off_qc, off_kc, off_qs, off_ks, off_mu, off_vc, off_vs, off_wqk, off_wv, off_wa;
-  size_t wqk, wv, wa, total;
+  size_t off_qi, off_ki, off_qs, off_ks, off_mu, off_vc, off_vs, off_wp;
+  size_t wp, total;
 };
 
 DeviceLayout device_layout(int B, int H, int Nq, int Nk) {
@@ -136,19 +134,15 @@ DeviceLayout device_layout(int B, int H, int Nq, int Nk) {
     off += up(bytes);
     return o;
   };
-  L.off_qc = take(BH * Nq * sg::kD);
-  L.off_kc = take(BH * Nk * sg::kD);
+  L.off_qi = take(BH * Nq * sg::kD * 2);
+  L.off_ki = take(BH * Nk * sg::kD * 2);
   L.off_qs = take(BH * sg::ceil_div(Nq, 64) * sizeof(float));  // blocks of 64 or 128 tokens
   L.off_ks = take(BH * sg::ceil_div(Nk, 64) * sizeof(float));
   L.off_mu = take(BH * sg::kD * sizeof(float));
   L.off_vc = take(BH * sg::kD * size_t(sg::nk_pad(Nk)));
   L.off_vs = take(BH * sg::kD * sizeof(float));
-  L.wqk = sage_quantize_qk_workspace(B, H, Nk);
-  L.wv = sage_quantize_v_workspace(B, H, Nk);
-  L.wa = sage_attn_fwd_workspace(B, H, Nq, Nk);
-  L.off_wqk = take(L.wqk);
-  L.off_wv = take(L.wv);
-  L.off_wa = take(L.wa);
+  L.wp = sage_quantize_qkv_workspace(B, H, Nk);
+  L.off_wp = take(L.wp);
   L.total = off + kAlign;  // room to align the base
   return L;
 }
@@ -182,19 +176,16 @@ sage_status sage_attention(const void *q_bf16, sage_strides qs, const void *k_bf
   if (workspace_bytes < L.total) return SAGE_ERR_WORKSPACE;
   uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(workspace) + kAlign - 1) &
                                             ~uintptr_t(kAlign - 1));
-  auto *qc = reinterpret_cast<int8_t *>(ws + L.off_qc);
-  auto *kc = reinterpret_cast<int8_t *>(ws + L.off_kc);
   auto *qsc = reinterpret_cast<float *>(ws + L.off_qs);
   auto *ksc = reinterpret_cast<float *>(ws + L.off_ks);
   auto *vc = reinterpret_cast<uint8_t *>(ws + L.off_vc);
   auto *vsc = reinterpret_cast<float *>(ws + L.off_vs);
-  sage_status r = sage_quantize_qk(q_bf16, qs, k_bf16, ks, B, H, Nq, Nk, sg::kD, q_block, k_block, qc, qsc, kc, ksc,
-                                   reinterpret_cast<float *>(ws + L.off_mu), ws + L.off_wqk, L.wqk, stream);
+  sage_status r = sage_quantize_qkv(q_bf16, qs, k_bf16, ks, v_bf16, vs, B, H, Nq, Nk, sg::kD, q_block, k_block,
+                                    SAGE_QK_F16, ws + L.off_qi, qsc, ws + L.off_ki, ksc,
+                                    reinterpret_cast<float *>(ws + L.off_mu), vc, vsc, ws + L.off_wp, L.wp, stream);
   if (r == SAGE_OK)
-    r = sage_quantize_v(v_bf16, vs, B, H, Nk, sg::kD, vc, vsc, ws + L.off_wv, L.wv, stream);
-  if (r == SAGE_OK)
-    r = sage_attn_fwd_ex(qc, qsc, kc, ksc, vc, vsc, B, H, Nq, Nk, sg::kD, q_block, k_block, sm_scale, causal,
-                         out_bf16, os, lse, ws + L.off_wa, L.wa, status_dev, stream);
+    r = sage_attn_fwd_f16(ws + L.off_qi, qsc, ws + L.off_ki, ksc, vc, vsc, B, H, Nq, Nk, sg::kD, q_block, k_block,
+                          sm_scale, causal, out_bf16, os, lse, status_dev, stream);
   return r;
 }
 
@@ -257,28 +248,21 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     ck(cudaMemcpyAsync(ws + L.off_in[s][2], static_cast<const uint8_t *>(v_host) + h0 * krow, n * krow,
                        cudaMemcpyHostToDevice, xs));
   };
-  // both quantizers of chunk c on the staging stream, then q_ready[c]
+  // the preparation of chunk c on the staging stream (fp16 images of the Q/K
+  // codes, so that only the attention kernel runs on the compute stream),
+  // then q_ready[c]
   auto quantize = [&](int c) {
     const int s = c & 1, n = heads_of(c);
-    sage_status r = sage_quantize_qk(ws + L.off_in[s][0], q_strides(n), ws + L.off_in[s][1], kv_strides(n), 1, n,
-                                     Nq, Nk, sg::kD, q_block, k_block, reinterpret_cast<int8_t *>(ws + L.off_qc[s]),
-                                     reinterpret_cast<float *>(ws + L.off_qs[s]),
-                                     reinterpret_cast<int8_t *>(ws + L.off_kc[s]),
-                                     reinterpret_cast<float *>(ws + L.off_ks[s]),
-                                     reinterpret_cast<float *>(ws + L.off_mu[s]), ws + L.off_wqk[s], L.wqk, xs);
-    if (r == SAGE_OK)
-      r = sage_quantize_v(ws + L.off_in[s][2], kv_strides(n), 1, n, Nk, sg::kD,
-                          reinterpret_cast<uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<float *>(ws + L.off_vs[s]),
-                          ws + L.off_wv[s], L.wv, xs);
+    const sage_status r = sage_quantize_qkv(
+        ws + L.off_in[s][0], q_strides(n), ws + L.off_in[s][1], kv_strides(n), ws + L.off_in[s][2], kv_strides(n), 1,
+        n, Nq, Nk, sg::kD, q_block, k_block, SAGE_QK_F16, ws + L.off_qi[s], reinterpret_cast<float *>(ws + L.off_qs[s]),
+        ws + L.off_ki[s], reinterpret_cast<float *>(ws + L.off_ks[s]), reinterpret_cast<float *>(ws + L.off_mu[s]),
+        reinterpret_cast<uint8_t *>(ws + L.off_vc[s]), reinterpret_cast<float *>(ws + L.off_vs[s]), ws + L.off_wp[s],
+        L.wp, xs);
     if (r != SAGE_OK) {
       fail(r);
       return;
     }
-    // the attention's fp16 images of the codes, so that only its kernel runs on the compute stream
-    ck(sg::launch_codes_to_f16(reinterpret_cast<const int8_t *>(ws + L.off_qc[s]), ws + L.off_qi[s],
-                               int64_t(n) * Nq * sg::kD, xs));
-    ck(sg::launch_codes_to_f16(reinterpret_cast<const int8_t *>(ws + L.off_kc[s]), ws + L.off_ki[s],
-                               int64_t(n) * Nk * sg::kD, xs));
     if (st == SAGE_OK) ck(cudaEventRecord(q_ready[c], xs));
   };
   for (int c = 0; c < 2 && c < C && st == SAGE_OK; ++c) {
@@ -290,9 +274,9 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     if (!ck(cudaStreamWaitEvent(cs, q_ready[c], 0))) break;
     // the attention kernel alone (arguments checked above; images written by the staging stream)
     sg::DenseArgs a;
-    a.q_codes = reinterpret_cast<const int8_t *>(ws + L.off_qc[s]);
+    a.q_codes = nullptr;  // the attention reads the images
     a.q_scales = reinterpret_cast<const float *>(ws + L.off_qs[s]);
-    a.k_codes = reinterpret_cast<const int8_t *>(ws + L.off_kc[s]);
+    a.k_codes = nullptr;
     a.k_scales = reinterpret_cast<const float *>(ws + L.off_ks[s]);
     a.v_codes = reinterpret_cast<const uint8_t *>(ws + L.off_vc[s]);
     a.v_scales = reinterpret_cast<const float *>(ws + L.off_vs[s]);
