@@ -369,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[32];
         // The tile's softmax; kMasked (keys past Nk in this tile) is a
         // compile-time flag so that full tiles carry no per-element predicates.
+        const int quad = warp & 3;
+        bool turn_ok = true;
         auto softmax_tile = [&](auto masked_c) {
           constexpr bool kMasked = decltype(masked_c)::value;
           if (kMasked) {
@@ -397,6 +399,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mnew = fmaxf(m, mt);
           alpha = (m == -INFINITY) ? 0.f : ex2(__fsub_rn(m, mnew));
+          // only the exponential phase takes turns with the other tile's warp
+          if (ntile == 2 && (t == 1 || j >= 1)) {
+            turn_ok = mbar_wait(&bars->turn[t][quad], (t == 1 ? j : j - 1) & 1, abort, p.wait_ns);
+            if (!turn_ok) return;
+          }
           // x = S * t - (m' - log2 448): 2^x = 448 * p
           const float nb = __fsub_rn(kLog2_448, mnew);
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
@@ -445,13 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for the arithmetic, so that one computes while the other loads S
         // or waits for its P.V, instead of both competing for issue slots
         // and then idling together.  Tile 0 goes first in every round.
-        const int quad = warp & 3;
-        if (ntile == 2 && (t == 1 || j >= 1)) {
-          ok = mbar_wait(&bars->turn[t][quad], (t == 1 ? j : j - 1) & 1, abort, p.wait_ns);
-          if (!ok) break;
-        }
         if (__any_sync(0xffffffffu, nvalid < BN)) softmax_tile(std::true_type{});
         else softmax_tile(std::false_type{});
+        if (!turn_ok) {
+          ok = false;
+          break;
+        }
         if (ntile == 2) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->turn[t ^ 1][quad]);
