@@ -54,12 +54,18 @@ METRIC = "quantized attention fwd effective TFLOPS (4*Nq*Nk*d*H), video-DiT 37,8
 UNIT = "TFLOP/s"
 WORKLOAD = "videodit_b1h24n37810"
 
-# dram bytes (read + write) per sage_attn_fwd call (two code->fp16 image
-# passes + the attention kernel), from one ncu capture of the 24-head,
-# 8192-token case scaled by 37810/8192 (every head's inputs are read once, so
-# the bytes grow with heads x tokens), for the kernel source with this sha256
-# prefix; None once the source has changed.
-TRAFFIC = {"sha256_prefix": "8c5862e9f02ab6e1", "bytes": 929.3e6}
+# DRAM bytes (read + write) per launch of the attention kernel, from one ncu
+# capture of the 24-head, 16,384-token case (the fp16 images exceed L2 there):
+# 251.8 MB read + 72.3 MB written, scaled by 37,810 / 16,384 (every head's
+# inputs are read once, so the bytes grow with heads x tokens); and the kernel's
+# tensor-pipe activity from the full ncu capture of the 8,192-token case.  Both
+# hold for the kernel source with this sha256 prefix and are None once the
+# source has changed.
+TRAFFIC = {"sha256_prefix": "3d17c4ba505833bb", "bytes": (251.8e6 + 72.3e6) * 37810 / 16384,
+           "tensor_pipe_active": 0.479}
+# algorithmic bytes of one attention launch at the full workload: Q, K, V codes
+# (1 byte per element) and the bf16 output
+ATTN_METHOD_BYTES = 24 * 37810 * 128 * (1 + 1 + 1 + 2)
 
 
 def peaks():
@@ -719,7 +725,8 @@ def run_ours(args, rank, world):
     peak_mixed = 2.0 / (1.0 / p16 + 1.0 / (2.0 * p16))
     achieved = w.flops / (comp["sage_attn_fwd_f16_ms"] * 1e-3) / 1e12
     sha = kernel_sha("attn_dense.cu")[:16]
-    traffic = TRAFFIC["bytes"] if TRAFFIC["sha256_prefix"] == sha else None
+    same_src = TRAFFIC["sha256_prefix"] == sha
+    traffic = TRAFFIC["bytes"] if same_src else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -732,6 +739,9 @@ def run_ours(args, rank, world):
         "roofline": {"kernel": "sage_attn_fwd_kernel (tcgen05 attention over the fp16 images, sage_attn_fwd_f16)",
                      "bound": "tensor", "achieved": achieved, "peak": peak_mixed, "unit": "TFLOP/s",
                      "frac": achieved / peak_mixed, "traffic": traffic,
+                     "algorithmic_bytes": ATTN_METHOD_BYTES,
+                     "traffic_ratio": traffic / ATTN_METHOD_BYTES if traffic else None,
+                     "tensor_pipe_active": TRAFFIC["tensor_pipe_active"] if same_src else None,
                      "peak_note": (f"{pk['source']}: bf16 burst {p16} TFLOP/s for the Q.K^T half, x2 (nominal "
                                    f"fp8/bf16 ratio) for the P.V half"),
                      # the softmax's MUFU demand: one ex2 per score
