@@ -36,7 +36,8 @@ namespace sg {
 namespace kv {
 
 constexpr int BM = 128, BN = 128, NSK = 2, NSV = 3;
-constexpr int kThreads = 256;
+constexpr int kHalf = BN / 2;  // keys of a tile per softmax warpgroup
+constexpr int kThreads = 384;
 constexpr uint32_t kQBytes = BM * kD * 2;
 constexpr uint32_t kKTile = BN * kD * 2;                // bf16 K image
 constexpr uint32_t kVBytes = kD * BN * 2;               // fp16 V^T image
@@ -47,13 +48,15 @@ constexpr uint32_t kOffV = kOffK + NSK * kKTile;
 constexpr uint32_t kOffKt = kOffV + NSV * kVBytes;
 constexpr uint32_t kOffVs = kOffKt + NSV * BN * 4;
 constexpr uint32_t kOffBar = kOffVs + NSV * BN * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+constexpr uint32_t kOffX = kOffBar + 256;  // (m, l) of both key halves per row, for the final merge
+constexpr uint32_t kSmemBytes = kOffX + 2 * BM * 8 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-// TMEM: S double buffer at columns 0 and 128, O at 256.  P_j (fp16 hi in the
-// first 64 columns, lo in the next 64) overwrites the consumed S_j buffer.
+// TMEM: S double buffer at columns 0 and 128; O of the two key halves at 256
+// and 384.  Half h's P (fp16 hi of its 64 keys in 32 columns, then lo in 32)
+// overwrites that half's own 64 columns of the consumed S buffer.
 __host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-constexpr uint32_t kColO = 256;
+__host__ __device__ constexpr uint32_t col_o(int h) { return h ? 384u : 256u; }
 
 constexpr uint32_t kIdescQK = make_idesc(kFmtF32, kFmtBF16, kFmtBF16, BM, BN);
 constexpr uint32_t kIdescPV = make_idesc(kFmtF32, kFmtF16, kFmtF16, BM, kD);
@@ -70,12 +73,12 @@ struct Params {
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  // p_full and pv_done per S/P buffer (tile j uses j & 1).  A softmax warp
-  // may finish tile j+1 before another warp finishes tile j (never two tiles,
-  // since QK(j+2) follows PV(j)), so one barrier per kind could be completed
-  // by the wrong tile's arrivals, and a parity wait on it could be answered
-  // by a phase two behind.
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  // s_full per S buffer (tile j uses j & 1); p_full and pv_done per key half
+  // and buffer.  A softmax warp may finish tile j+1 before another finishes
+  // tile j (never two tiles, since QK(j+2) follows PV(j)), so one barrier per
+  // kind could be completed by the wrong tile's arrivals.
+  uint64_t s_full[2], p_full[2][2], pv_done[2][2];
+  uint64_t merged;  // both halves' final (m, l) are in shared memory
   uint32_t tmem_base;
   int abort;
 };
@@ -91,12 +94,20 @@ __device__ __forceinline__ int kv_tiles_for(const Params &p, int qtile) {
   return last_key / BN + 1;
 }
 
+// Roles: warp 0 TMA, warp 1 MMA; warps 4-7 the softmax of keys 0-63 of every
+// tile (half 0) and warps 8-11 of keys 64-127 (half 1), one query row per
+// thread (TMEM lane = row).  The halves run independent online softmaxes
+// (their own running max, sum and O accumulator) and merge once at the end;
+// the oracle of this path is the exact softmax, so splitting the keys only
+// changes the fp32 summation order.  Two softmax warps per sub-partition, no
+// exchange between them per tile.
 __global__ void __launch_bounds__(kThreads, 1)
     int8kv_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
+  float2 *xchg = reinterpret_cast<float2 *>(smem + kOffX);  // [half][row]
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, qtile = blockIdx.y, g = blockIdx.z;
@@ -117,12 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    mbar_init(&bars->s_full[0], 1);
-    mbar_init(&bars->s_full[1], 1);
-    mbar_init(&bars->p_full[0], 4);
-    mbar_init(&bars->p_full[1], 4);
-    mbar_init(&bars->pv_done[0], 1);
-    mbar_init(&bars->pv_done[1], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&bars->p_full[h][b], 4);
+        mbar_init(&bars->pv_done[h][b], 1);
+      }
+    }
+    mbar_init(&bars->merged, 8);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -137,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T <= 0) {
     // empty key range: record an empty partial for the combine
-    if (warp >= 4) {
+    if (warp >= 4 && warp < 8) {
       const int r = (warp - 4) * 32 + lane;
       p.part_ml[int64_t(unit) * BM + r] = make_float2(-INFINITY, 0.f);
     }
@@ -202,9 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((!ok || !drained) && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (converged warp)
-    // Order: QK(0), QK(1), then per tile j: PV(j) (A = P_j from TMEM), QK(j+2)
-    // into the same TMEM buffer (MMAs of one thread execute in order, so
-    // QK(j+2) overwrites P_j only after PV(j) has read it).
+    // Order: QK(0), QK(1), then per tile j: PV of half 0 and of half 1 (A =
+    // that half's P from TMEM), QK(j+2) into the same TMEM buffer (MMAs of one
+    // thread execute in order, so QK(j+2) overwrites P_j only after both P.V
+    // have read it).
     const bool leader = elect_one();
     const uint32_t sQ = smem_u32(smem + kOffQ);
     // the barrier and phase parity of the last commit (it covers every MMA
@@ -232,28 +246,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0) && (T < 2 || issue_qk(1));
     for (int j = 0; ok && j < T; ++j) {
-      const int s = j % NSV;
-      ok = mbar_wait(&bars->p_full[j & 1], (j >> 1) & 1, abort) && mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
-      if (!ok) break;
-      tc_fence_after();
+      const int s = j % NSV, b = j & 1;
+      ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
       const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
-      if (leader) {
-        // O += [P_hi | P_lo] . [V ; V]: 8 K-steps over P_hi then 8 over P_lo
+      for (int h = 0; ok && h < 2; ++h) {
+        ok = mbar_wait(&bars->p_full[h][b], (j >> 1) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+          // O_h += [P_hi | P_lo] . [V_h ; V_h]: 4 K-steps over P_hi, 4 over
+          // P_lo, both against the 64 keys of half h (the second 64-key block
+          // of the V^T tile for h = 1)
 #pragma unroll
-        for (int hl = 0; hl < 2; ++hl) {
-#pragma unroll
-          for (int k = 0; k < BN / 16; ++k) {
-            const uint32_t off = (k >> 2) * (kVBytes / 2) + (k & 3) * 32;
-            umma_f16_ts(tmem + kColO, tmem + col_s(j & 1) + 64 * hl + 8 * k, sdesc_sw128(sV + off), kIdescPV,
-                        (j > 0) || (hl > 0) || (k > 0));
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = h * (kVBytes / 2) + (k & 3) * 32;
+            umma_f16_ts(tmem + col_o(h), tmem + col_s(b) + kHalf * h + 8 * k, sdesc_sw128(sV + off), kIdescPV,
+                        (j > 0) || (k > 0));
           }
+          tc_commit(&bars->pv_done[h][b]);
         }
-        tc_commit(&bars->pv_done[j & 1]);
-        tc_commit(&bars->v_empty[s]);
+        __syncwarp();
+        last_bar = &bars->pv_done[h][b];
+        last_par = (j >> 1) & 1;
       }
+      if (!ok) break;
+      if (leader) tc_commit(&bars->v_empty[s]);
       __syncwarp();
-      last_bar = &bars->pv_done[j & 1];
-      last_par = (j >> 1) & 1;
       if (j + 2 < T) ok = issue_qk(j + 2);
     }
     // the MMAs read shared memory and write TMEM: wait for the last commit
@@ -261,13 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (last_bar != nullptr && !mbar_drain(last_bar, last_par)) ok = false;
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax / rescale / partials
-    const int r = (warp - 4) * 32 + lane;
+    // ------------------------------------------------------------ softmax of one key half
+    const int h = (warp - 4) >> 2;
+    const int r = (warp & 3) * 32 + lane;
     const int il = r / p.G;
     const int qi = i0 + il;
     const bool valid = (il < p.QT) && (qi < p.Nq);
     const int pos = p.q_pos0 + qi;  // keys 0..pos are visible
     const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+    const uint32_t colO = lane_base + col_o(h);
     // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16.  The
     // factor 2^-E is taken into the exponent (p' = 2^(s - m - E)), so the row
     // sum is l * 2^-E as well and O / l is unchanged.
@@ -277,60 +297,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      ok = mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1, abort);
+      const int b = j & 1;
+      ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sa = lane_base + col_s(j & 1);
-      uint32_t S[128];
+      const uint32_t sa = lane_base + col_s(b) + kHalf * h;
+      uint32_t S[kHalf];
       tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
       tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
-      tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
-      tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
-      const int key0 = (tb + j) * BN;
-      const int nvis = min(BN, pos - key0 + 1);  // visible keys of this tile (<= 0: none)
+      const int key0 = (tb + j) * BN + kHalf * h;
+      const int nvis = min(kHalf, pos - key0 + 1);  // visible keys of this half (<= 0: none)
       // kt and vs of this tile arrived with V(j); its slot is reused only
-      // after PV(j), which waits for this warp's p_full
+      // after both P.V of tile j, which wait for this warp's p_full
       const int sv = j % NSV;
       ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
       if (!ok) break;
-      const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4);
-      const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4);
+      const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4) + kHalf / 4 * h;
+      const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4) + kHalf / 4 * h;
       tmem_ld_wait(S);
       float *Sf = reinterpret_cast<float *>(S);
       float mnew, alpha, rowsum;
-      // The tile's softmax; kMasked (some row of the warp sees only part of
-      // the tile) is a compile-time flag so that the tiles below the diagonal
-      // carry no per-element predicates.
-      auto softmax_tile = [&](auto masked_c) {
+      // The half tile's softmax; kMasked (some row of the warp sees only part
+      // of the half) is a compile-time flag so that the tiles below the
+      // diagonal carry no per-element predicates.
+      auto softmax_half = [&](auto masked_c) {
         constexpr bool kMasked = decltype(masked_c)::value;
         // s = S * kt (base-2 logits)
 #pragma unroll
-        for (int i = 0; i < 128; i += 4) {
+        for (int i = 0; i < kHalf; i += 4) {
           const float4 k4 = kt4[i >> 2];
           const float2 a = fmul2(make_float2(Sf[i], Sf[i + 1]), make_float2(k4.x, k4.y));
-          const float2 b = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
+          const float2 c = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
           Sf[i] = a.x;
           Sf[i + 1] = a.y;
-          Sf[i + 2] = b.x;
-          Sf[i + 3] = b.y;
+          Sf[i + 2] = c.x;
+          Sf[i + 3] = c.y;
         }
         if (kMasked) {  // keys past the query's position
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
+          for (int i = 0; i < kHalf; ++i)
             if (i >= nvis) Sf[i] = -INFINITY;
         }
-        // row maximum, four independent chains
+        // row maximum, two independent chains
         float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
-        float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
 #pragma unroll
         for (int i = 3; i < 31; i += 2) {
           c0 = fmax3(c0, Sf[i], Sf[i + 1]);
           c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
-          c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
-          c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
         }
-        const float mt = fmaxf(fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]),
-                               fmax3(fmax3(c2, c3, Sf[95]), Sf[127], Sf[127]));
+        const float mt = fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]);
         mnew = fmaxf(m, mt);
         alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
         // x = s - (m' + E); masked entries stay -inf (p' = 0)
@@ -338,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 nb2 = make_float2(nb, nb);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
         // p' = 2^x, row sum, w = p' * vs split into fp16 hi + lo, written over
-        // this S buffer: hi at columns 0-63, lo at 64-127
+        // this half's S columns: hi at +0..31, lo at +32..63
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
@@ -373,62 +388,81 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
           }
           tmem_st16(sa + 16 * c, hi);
-          tmem_st16(sa + 64 + 16 * c, lo);
+          tmem_st16(sa + 32 + 16 * c, lo);
         }
         rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
       };
-      if (__any_sync(0xffffffffu, nvis < BN)) softmax_tile(std::true_type{});
-      else softmax_tile(std::false_type{});
+      if (__any_sync(0xffffffffu, nvis < kHalf)) softmax_half(std::true_type{});
+      else softmax_half(std::false_type{});
       l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
-      // O is stable once PV(j-1) is complete; rescale it when the max grew
+      // O_h is stable once its P.V of tile j-1 is complete; rescale it when
+      // this half's max grew (two round trips of 64 columns)
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+        ok = mbar_wait(&bars->pv_done[h][(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
         if (!ok) break;
         tc_fence_after();
-        // one load round trip and one store round trip for the 128 columns
-        uint32_t o[128];
-        tmem_ld32(lane_base + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_ld32(lane_base + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_ld32(lane_base + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
-        tmem_ld32(lane_base + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
-        tmem_ld_wait(o);
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int i = 0; i < 128; i += 2) {
-          const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-          o[i] = __float_as_uint(v.x);
-          o[i + 1] = __float_as_uint(v.y);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t o[64];
+          tmem_ld32(colO + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_ld32(colO + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            o[i] = __float_as_uint(v.x);
+            o[i + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(colO + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+          tmem_st32(colO + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
         }
-        tmem_st32(lane_base + kColO + 0, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_st32(lane_base + kColO + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_st32(lane_base + kColO + 64, *reinterpret_cast<uint32_t(*)[32]>(&o[64]));
-        tmem_st32(lane_base + kColO + 96, *reinterpret_cast<uint32_t(*)[32]>(&o[96]));
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full[h][j & 1]);
       m = mnew;
     }
-    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    if (ok) ok = mbar_wait(&bars->pv_done[h][(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    if (ok) {
+      // merge the two halves of the row: M = max(m_0, m_1), a_h = 2^(m_h - M),
+      // L = a_0 l_0 + a_1 l_1, O = a_0 O_0 + a_1 O_1; each half writes 64 of
+      // the 128 channels, half 0 also (M, L)
+      xchg[h * BM + r] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->merged);
+      ok = mbar_wait(&bars->merged, 0, abort);
+    }
     if (!ok) {
       report(p.status, SAGE_ERR_TIMEOUT);
     } else {
       tc_fence_after();
-      float *dst = p.part_o + (int64_t(unit) * BM + r) * kD;
+      const float2 h0 = xchg[r], h1 = xchg[BM + r];
+      const float M = fmaxf(h0.x, h1.x);
+      const float a0 = h0.x == -INFINITY ? 0.f : ex2(__fsub_rn(h0.x, M));
+      const float a1 = h1.x == -INFINITY ? 0.f : ex2(__fsub_rn(h1.x, M));
+      float *dst = p.part_o + (int64_t(unit) * BM + r) * kD + 64 * h;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + kColO + 32 * c, o);
-        tmem_ld_wait(o);
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(lane_base + col_o(0) + 64 * h + 32 * c, o0);
+        tmem_ld32(lane_base + col_o(1) + 64 * h + 32 * c, o1);
+        tmem_ld_wait(o0);
+        tmem_ld_wait(o1);
         if (valid) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4 *>(dst + 32 * c + 4 * u) =
-                make_uint4(o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+          for (int u = 0; u < 8; ++u) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              v[e] = __fadd_rn(__fmul_rn(a0, __uint_as_float(o0[4 * u + e])),
+                               __fmul_rn(a1, __uint_as_float(o1[4 * u + e])));
+            *reinterpret_cast<float4 *>(dst + 32 * c + 4 * u) = make_float4(v[0], v[1], v[2], v[3]);
+          }
         }
       }
-      p.part_ml[int64_t(unit) * BM + r] = make_float2(m, l);
+      if (h == 0) p.part_ml[int64_t(unit) * BM + r] = make_float2(M, __fadd_rn(__fmul_rn(a0, h0.y), __fmul_rn(a1, h1.y)));
     }
   }
   tc_fence_before();
