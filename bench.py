@@ -403,9 +403,11 @@ def run_reference(args, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded SplitMix64/Box-Muller, the workload's shapes)",
         "config": {"workload": WORKLOAD, "B": 1, "H": 24, "Nq": 37810, "Nk": 37810, "d": 128, "block": 128,
-                   "note": "CPU oracle (plain C, OpenMP) on a bounded sample, scaled to the workload"},
+                   "note": ("CPU oracle (plain C, OpenMP) on a bounded sample, scaled to the workload: "
+                            "ms_per_step is that extrapolation, not a timed run")},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": last["cores"], "kind": "oracle",
-                         "sample": last["sample"]},
+                         "sample": last["sample"], "extrapolated": True},
+        "extrapolated": True,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
