@@ -10,7 +10,10 @@
 //  * One 128-row tile holds QT = floor(128 / G) queries x the G query heads of
 //    one kv head (G = Hq / Hkv), so each K/V tile read serves all G heads.
 //  * S = Q.K^T on tcgen05 kind::f16 (bf16 queries x exact bf16 images of the
-//    int8 K codes), fp32 in TMEM.
+//    int8 K codes), fp32 in TMEM.  Q is copied into TMEM once per CTA and read
+//    from there (A operand): the MMAs that read both operands from shared
+//    memory take all of its bandwidth while they run, and the TMA copies of
+//    the next K/V tiles and the scale loads share it.
 //  * softmax per row in fp32: s = S * fl(ks * sm_scale * log2 e), causal mask
 //    by absolute position, p = 2^(s - m).
 //  * P.V: the weight w = p * vs (scaled by a power of two so that w < 1) is
@@ -18,6 +21,12 @@
 //    V codes by one K = 256 kind::f16 MMA chain ([hi | lo] . [V ; V]), so the
 //    fp16 rounding of w does not reach the output.  hi and lo are written
 //    with tcgen05.st over the consumed S buffer and read by the MMA from TMEM.
+//  * Four softmax warpgroups, one per 32-key quarter of every key tile, one
+//    query row per thread: four warps per SM sub-partition.  They share one
+//    O accumulator and one running max per row: each quarter's maximum is
+//    exchanged through shared memory under a named barrier of the four warps
+//    that hold the same rows, so every warpgroup uses the exact row maximum,
+//    and each rescales its own 32 columns of O.
 //  * S is double-buffered in TMEM and QK(j+2) is issued right behind PV(j),
 //    so the next scores are ready when the softmax finishes a tile; the MMA
 //    and TMA warps run converged with one elected lane issuing.
@@ -35,28 +44,37 @@
 namespace sg {
 namespace kv {
 
-constexpr int BM = 128, BN = 128, NSK = 2, NSV = 3;
-constexpr int kHalf = BN / 2;  // keys of a tile per softmax warpgroup
-constexpr int kThreads = 384;
+constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
+constexpr int kQuarter = BN / 4;  // keys of a tile per softmax warpgroup
+// warp 0 TMA, warp 1 MMA, warps 2-17 softmax (quarter (w - 2) / 4, TMEM lane
+// quadrant w % 4: four consecutive warps cover the four quadrants)
+constexpr int kSoftmaxWarp0 = 2;
+constexpr int kThreads = (kSoftmaxWarp0 + 16) * 32;
 constexpr uint32_t kQBytes = BM * kD * 2;
 constexpr uint32_t kKTile = BN * kD * 2;                // bf16 K image
 constexpr uint32_t kVBytes = kD * BN * 2;               // fp16 V^T image
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kQBytes;
-constexpr uint32_t kOffV = kOffK + NSK * kKTile;
+constexpr uint32_t kOffV = kOffK + 2 * kKTile;
+// K ring: stages 0 and 1 at kOffK, stage 2 in the Q tile, which is free once
+// Q has been copied into TMEM
+__host__ __device__ constexpr uint32_t k_stage(int s) { return s == 2 ? kOffQ : kOffK + uint32_t(s) * kKTile; }
 // the tile's kt and vs (128 fp32 each) ride with its V tile
 constexpr uint32_t kOffKt = kOffV + NSV * kVBytes;
 constexpr uint32_t kOffVs = kOffKt + NSV * BN * 4;
 constexpr uint32_t kOffBar = kOffVs + NSV * BN * 4;
-constexpr uint32_t kOffX = kOffBar + 256;  // (m, l) of both key halves per row, for the final merge
-constexpr uint32_t kSmemBytes = kOffX + 2 * BM * 8 + 1024;
+// per row and quarter: the quarter maxima of a tile (two tiles in flight) and
+// the final partial row sums
+constexpr uint32_t kOffXm = kOffBar + 256;
+constexpr uint32_t kOffXl = kOffXm + 2 * BM * 4 * 4;
+constexpr uint32_t kSmemBytes = kOffXl + BM * 4 * 4 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
-// TMEM: S double buffer at columns 0 and 128; O of the two key halves at 256
-// and 384.  Half h's P (fp16 hi of its 64 keys in 32 columns, then lo in 32)
-// overwrites that half's own 64 columns of the consumed S buffer.
+// TMEM: S double buffer at columns 0 and 128, O at 256, Q (bf16 pairs) at
+// 384-447.  Quarter g's P (fp16 hi of its 32 keys in 16 columns, then lo in
+// 16) overwrites that quarter's own 32 columns of the consumed S buffer.
 __host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t col_o(int h) { return h ? 384u : 256u; }
+constexpr uint32_t kColO = 256, kColQ = 384;
 
 constexpr uint32_t kIdescQK = make_idesc(kFmtF32, kFmtBF16, kFmtBF16, BM, BN);
 constexpr uint32_t kIdescPV = make_idesc(kFmtF32, kFmtF16, kFmtF16, BM, kD);
@@ -71,14 +89,13 @@ struct Params {
 };
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full, q_tmem;  // Q in shared memory; Q copied into TMEM
   uint64_t k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV];
-  // s_full per S buffer (tile j uses j & 1); p_full and pv_done per key half
-  // and buffer.  A softmax warp may finish tile j+1 before another finishes
-  // tile j (never two tiles, since QK(j+2) follows PV(j)), so one barrier per
-  // kind could be completed by the wrong tile's arrivals.
-  uint64_t s_full[2], p_full[2][2], pv_done[2][2];
-  uint64_t merged;  // both halves' final (m, l) are in shared memory
+  // s_full, p_full and pv_done per S buffer (tile j uses j & 1): a softmax
+  // warp may finish tile j+1 before another finishes tile j (never two
+  // tiles: the quarters meet at a named barrier every tile), so one barrier
+  // per kind could be completed by the wrong tile's arrivals.
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -94,20 +111,21 @@ __device__ __forceinline__ int kv_tiles_for(const Params &p, int qtile) {
   return last_key / BN + 1;
 }
 
-// Roles: warp 0 TMA, warp 1 MMA; warps 4-7 the softmax of keys 0-63 of every
-// tile (half 0) and warps 8-11 of keys 64-127 (half 1), one query row per
-// thread (TMEM lane = row).  The halves run independent online softmaxes
-// (their own running max, sum and O accumulator) and merge once at the end;
-// the oracle of this path is the exact softmax, so splitting the keys only
-// changes the fp32 summation order.  Two softmax warps per sub-partition, no
-// exchange between them per tile.
+// Roles: warp 0 TMA, warp 1 MMA; warps 2-17 the softmax, warp w taking key
+// quarter (w - 2) / 4 of every tile for the 32 query rows of TMEM lane
+// quadrant w % 4, one row per thread (TMEM lane = row).  The four quarters of
+// a row agree on the row maximum every tile (named barrier 1 + quadrant) and
+// keep partial row sums that are added in quarter order at the end; the
+// oracle of this path is the exact softmax, so splitting the keys only
+// changes the fp32 summation order.
 __global__ void __launch_bounds__(kThreads, 1)
     int8kv_attn_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + kOffBar);
-  float2 *xchg = reinterpret_cast<float2 *>(smem + kOffX);  // [half][row]
+  float4 *xm = reinterpret_cast<float4 *>(smem + kOffXm);  // [tile & 1][row]: the four quarter maxima
+  float4 *xl = reinterpret_cast<float4 *>(smem + kOffXl);  // [row]: the four partial row sums
   volatile int *abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, qtile = blockIdx.y, g = blockIdx.z;
@@ -120,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_tmem, 4);  // the four warps of quarter 0
     for (int s = 0; s < NSK; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->k_empty[s], 1);
@@ -130,12 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
-      for (int h = 0; h < 2; ++h) {
-        mbar_init(&bars->p_full[h][b], 4);
-        mbar_init(&bars->pv_done[h][b], 1);
-      }
+      mbar_init(&bars->p_full[b], 16);  // one arrive per softmax warp
+      mbar_init(&bars->pv_done[b], 1);
     }
-    mbar_init(&bars->merged, 8);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -150,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T <= 0) {
     // empty key range: record an empty partial for the combine
-    if (warp >= 4 && warp < 8) {
-      const int r = (warp - 4) * 32 + lane;
+    if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+      const int r = (warp & 3) * 32 + lane;
       p.part_ml[int64_t(unit) * BM + r] = make_float2(-INFINITY, 0.f);
     }
   } else if (warp == 0) {
@@ -170,9 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_k = [&](int j) -> bool {
       const int s = j % NSK;
       if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
+      if (j == 2 && !mbar_wait(&bars->q_tmem, 0, abort)) return false;  // stage 2 is the Q tile
       if (leader) {
         const int key0 = (tb + j) * BN;
-        uint8_t *dst = smem + kOffK + s * kKTile;
+        uint8_t *dst = smem + k_stage(s);
         mbar_arrive_expect_tx(&bars->k_full[s], kKTile);
         tma_load_3d(dst, &tmK, &bars->k_full[s], 0, key0, g);
         tma_load_3d(dst + kKTile / 2, &tmK, &bars->k_full[s], 64, key0, g);
@@ -198,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++nv;
       return true;
     };
-    // order of first use: K0, K1, V0, K2, V1, K3, ...
+    // order of first use: K0, K1, V0, K2, V1, K3, ...; K(j+2) waits for the
+    // Q.K^T of tile j-1, one tile earlier than a two-stage ring would
     bool ok = load_k(0) && (T < 2 || load_k(1));
     for (int j = 0; ok && j < T; ++j) {
       ok = load_v(j);
@@ -215,12 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if ((!ok || !drained) && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (converged warp)
-    // Order: QK(0), QK(1), then per tile j: PV of half 0 and of half 1 (A =
-    // that half's P from TMEM), QK(j+2) into the same TMEM buffer (MMAs of one
-    // thread execute in order, so QK(j+2) overwrites P_j only after both P.V
-    // have read it).
+    // Order: QK(0), QK(1), then per tile j: PV (A = the four quarters' P from
+    // TMEM), QK(j+2) into the same TMEM buffer (MMAs of one thread execute in
+    // order, so QK(j+2) overwrites P_j only after P.V has read it).
     const bool leader = elect_one();
-    const uint32_t sQ = smem_u32(smem + kOffQ);
     // the barrier and phase parity of the last commit (it covers every MMA
     // issued before it)
     uint64_t *last_bar = nullptr;
@@ -229,12 +245,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = j % NSK;
       if (!mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort)) return false;
       tc_fence_after();
-      const uint32_t sK = smem_u32(smem + kOffK + s * kKTile);
+      const uint32_t sK = smem_u32(smem + k_stage(s));
       if (leader) {
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kQBytes / 2) + (k & 3) * 32;
-          umma_f16(tmem + col_s(j & 1), sdesc_sw128(sQ + off), sdesc_sw128(sK + off), kIdescQK, k > 0);
+          const uint32_t off = (k >> 2) * (kKTile / 2) + (k & 3) * 32;
+          umma_f16_ts(tmem + col_s(j & 1), tmem + kColQ + 8 * k, sdesc_sw128(sK + off), kIdescQK, k > 0);
         }
         tc_commit(&bars->s_full[j & 1]);
         tc_commit(&bars->k_empty[s]);
@@ -244,87 +260,119 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_par = (j >> 1) & 1;
       return true;
     };
-    bool ok = mbar_wait(&bars->q_full, 0, abort) && issue_qk(0) && (T < 2 || issue_qk(1));
+    bool ok = mbar_wait(&bars->q_tmem, 0, abort);
+    tc_fence_after();
+    ok = ok && issue_qk(0) && (T < 2 || issue_qk(1));
     for (int j = 0; ok && j < T; ++j) {
       const int s = j % NSV, b = j & 1;
-      ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort);
-      const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
-      for (int h = 0; ok && h < 2; ++h) {
-        ok = mbar_wait(&bars->p_full[h][b], (j >> 1) & 1, abort);
-        if (!ok) break;
-        tc_fence_after();
-        if (leader) {
-          // O_h += [P_hi | P_lo] . [V_h ; V_h]: 4 K-steps over P_hi, 4 over
-          // P_lo, both against the 64 keys of half h (the second 64-key block
-          // of the V^T tile for h = 1)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = h * (kVBytes / 2) + (k & 3) * 32;
-            umma_f16_ts(tmem + col_o(h), tmem + col_s(b) + kHalf * h + 8 * k, sdesc_sw128(sV + off), kIdescPV,
-                        (j > 0) || (k > 0));
-          }
-          tc_commit(&bars->pv_done[h][b]);
-        }
-        __syncwarp();
-        last_bar = &bars->pv_done[h][b];
-        last_par = (j >> 1) & 1;
-      }
+      ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort) && mbar_wait(&bars->p_full[b], (j >> 1) & 1, abort);
       if (!ok) break;
-      if (leader) tc_commit(&bars->v_empty[s]);
+      tc_fence_after();
+      const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
+      if (leader) {
+        // O += sum over quarters g of [P_hi,g | P_lo,g] . [V_g ; V_g]: per
+        // quarter two K-steps of 16 keys over hi and two over lo, against
+        // keys 32g..32g+31 of the V^T tile (64-key blocks 16 KB apart,
+        // 16 keys = 32 bytes of a 128-byte swizzled row)
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t off = (g >> 1) * (kVBytes / 2) + ((g & 1) * 2 + (k & 1)) * 32;
+            umma_f16_ts(tmem + kColO, tmem + col_s(b) + kQuarter * g + 8 * k, sdesc_sw128(sV + off), kIdescPV,
+                        (j > 0) || (g > 0) || (k > 0));
+          }
+        }
+        tc_commit(&bars->pv_done[b]);
+        tc_commit(&bars->v_empty[s]);
+      }
       __syncwarp();
+      last_bar = &bars->pv_done[b];
+      last_par = (j >> 1) & 1;
       if (j + 2 < T) ok = issue_qk(j + 2);
     }
     // the MMAs read shared memory and write TMEM: wait for the last commit
     // before the CTA may free either
     if (last_bar != nullptr && !mbar_drain(last_bar, last_par)) ok = false;
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax of one key half
-    const int h = (warp - 4) >> 2;
-    const int r = (warp & 3) * 32 + lane;
+  } else if (warp >= kSoftmaxWarp0) {
+    // ------------------------------------------------------------ softmax of one key quarter
+    const int g = (warp - kSoftmaxWarp0) >> 2;  // key quarter
+    const int quad = warp & 3;                  // TMEM lane quadrant
+    const int r = quad * 32 + lane;
     const int il = r / p.G;
     const int qi = i0 + il;
     const bool valid = (il < p.QT) && (qi < p.Nq);
     const int pos = p.q_pos0 + qi;  // keys 0..pos are visible
-    const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
-    const uint32_t colO = lane_base + col_o(h);
+    const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
+    const uint32_t colO = lane_base + kColO + kQuarter * g;  // this quarter's 32 columns of O
     // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16.  The
     // factor 2^-E is taken into the exponent (p' = 2^(s - m - E)), so the row
     // sum is l * 2^-E as well and O / l is unchanged.
     const float vmax = __uint_as_float(*p.vmax_bits);
     const int E = vmax > 0.f ? int((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
     const float Ef = float(E);
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // m: the row's running max (same in all quarters); l: this quarter's sum
     bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    // Named barriers cannot time out, so every warp of a quadrant passes
+    // exactly T + 1 of them (one per tile and one at the end), also after a
+    // bounded wait gave up: a warp that left the loop early makes up the
+    // ones it skipped, without work, so that the others are never stranded.
+    int nbar = 0;
+    if (g == 0) {
+      // Q into TMEM: row r's 128 bf16 (two 128-byte swizzled rows of the TMA
+      // boxes; 16-byte chunk c of row r sits at chunk c ^ (r & 7)) become 64
+      // columns of bf16 pairs, the A-operand layout of Q.K^T
+      ok = mbar_wait(&bars->q_full, 0, abort);
+      if (ok) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint8_t *row = smem + kOffQ + half * (kQBytes / 2) + r * 128;
+          uint32_t qw[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((c ^ (r & 7)) << 4));
+            qw[4 * c] = v.x;
+            qw[4 * c + 1] = v.y;
+            qw[4 * c + 2] = v.z;
+            qw[4 * c + 3] = v.w;
+          }
+          tmem_st32(lane_base + kColQ + 32 * half, qw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->q_tmem);
+      }
+    }
+    for (int j = 0; ok && j < T; ++j) {
       const int b = j & 1;
       ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t sa = lane_base + col_s(b) + kHalf * h;
-      uint32_t S[kHalf];
-      tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
-      tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
-      const int key0 = (tb + j) * BN + kHalf * h;
-      const int nvis = min(kHalf, pos - key0 + 1);  // visible keys of this half (<= 0: none)
+      const uint32_t sa = lane_base + col_s(b) + kQuarter * g;
+      uint32_t S[kQuarter];
+      tmem_ld32(sa, S);
+      const int key0 = (tb + j) * BN + kQuarter * g;
+      const int nvis = min(kQuarter, pos - key0 + 1);  // visible keys of this quarter (<= 0: none)
       // kt and vs of this tile arrived with V(j); its slot is reused only
-      // after both P.V of tile j, which wait for this warp's p_full
+      // after the P.V of tile j, which waits for this warp's p_full
       const int sv = j % NSV;
       ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
       if (!ok) break;
-      const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4) + kHalf / 4 * h;
-      const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4) + kHalf / 4 * h;
+      const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4) + kQuarter / 4 * g;
+      const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4) + kQuarter / 4 * g;
       tmem_ld_wait(S);
       float *Sf = reinterpret_cast<float *>(S);
       float mnew, alpha, rowsum;
-      // The half tile's softmax; kMasked (some row of the warp sees only part
-      // of the half) is a compile-time flag so that the tiles below the
-      // diagonal carry no per-element predicates.
-      auto softmax_half = [&](auto masked_c) {
+      // The quarter tile's softmax; kMasked (some row of the warp sees only
+      // part of the quarter) is a compile-time flag so that the tiles below
+      // the diagonal carry no per-element predicates.
+      auto softmax_quarter = [&](auto masked_c) {
         constexpr bool kMasked = decltype(masked_c)::value;
         // s = S * kt (base-2 logits)
 #pragma unroll
-        for (int i = 0; i < kHalf; i += 4) {
+        for (int i = 0; i < kQuarter; i += 4) {
           const float4 k4 = kt4[i >> 2];
           const float2 a = fmul2(make_float2(Sf[i], Sf[i + 1]), make_float2(k4.x, k4.y));
           const float2 c = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
@@ -335,17 +383,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kMasked) {  // keys past the query's position
 #pragma unroll
-          for (int i = 0; i < kHalf; ++i)
+          for (int i = 0; i < kQuarter; ++i)
             if (i >= nvis) Sf[i] = -INFINITY;
         }
-        // row maximum, two independent chains
-        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
+        // the quarter's maximum (two chains), then the row's over all four
+        // quarters: the four warps holding these rows meet at named barrier
+        // 1 + quad; xm is double-buffered by tile, and no warp can be two
+        // tiles ahead of another since each tile has such a barrier
+        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[16], Sf[17], Sf[18]);
 #pragma unroll
-        for (int i = 3; i < 31; i += 2) {
+        for (int i = 3; i < 15; i += 2) {
           c0 = fmax3(c0, Sf[i], Sf[i + 1]);
-          c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
+          c1 = fmax3(c1, Sf[16 + i], Sf[17 + i]);
         }
-        const float mt = fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]);
+        const float mq = fmax3(fmax3(c0, c1, Sf[15]), Sf[31], Sf[31]);
+        reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
+        named_bar_sync(1 + quad, 128);
+        ++nbar;
+        const float4 mx = xm[b * BM + r];
+        const float mt = fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w));
         mnew = fmaxf(m, mt);
         alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
         // x = s - (m' + E); masked entries stay -inf (p' = 0)
@@ -353,13 +409,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 nb2 = make_float2(nb, nb);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
         // p' = 2^x, row sum, w = p' * vs split into fp16 hi + lo, written over
-        // this half's S columns: hi at +0..31, lo at +32..63
+        // this quarter's S columns: hi at +0..15, lo at +16..31
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t hi[16], lo[16];
+          uint32_t hi[8], lo[8];
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const int e = 32 * c + i;
+          for (int i = 0; i < 16; i += 4) {
+            const int e = 16 * c + i;
             const float4 v4 = vs4[e >> 2];
             const float2 x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
             const float2 x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
@@ -387,82 +443,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
             lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
           }
-          tmem_st16(sa + 16 * c, hi);
-          tmem_st16(sa + 32 + 16 * c, lo);
+          tmem_st8(sa + 8 * c, hi);
+          tmem_st8(sa + 16 + 8 * c, lo);
         }
         rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
       };
-      if (__any_sync(0xffffffffu, nvis < kHalf)) softmax_half(std::true_type{});
-      else softmax_half(std::false_type{});
+      if (__any_sync(0xffffffffu, nvis < kQuarter)) softmax_quarter(std::true_type{});
+      else softmax_quarter(std::false_type{});
       l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
-      // O_h is stable once its P.V of tile j-1 is complete; rescale it when
-      // this half's max grew (two round trips of 64 columns)
+      // O is stable once the P.V of tile j-1 is complete; this quarter's
+      // warps rescale their 32 columns of it when the row max grew
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = mbar_wait(&bars->pv_done[h][(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
         if (!ok) break;
         tc_fence_after();
+        uint32_t o[32];
+        tmem_ld32(colO, o);
+        tmem_ld_wait(o);
         const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t o[64];
-          tmem_ld32(colO + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          tmem_ld32(colO + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) {
-            const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-            o[i] = __float_as_uint(v.x);
-            o[i + 1] = __float_as_uint(v.y);
-          }
-          tmem_st32(colO + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-          tmem_st32(colO + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        for (int i = 0; i < 32; i += 2) {
+          const float2 v = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+          o[i] = __float_as_uint(v.x);
+          o[i + 1] = __float_as_uint(v.y);
         }
+        tmem_st32(colO, o);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[h][j & 1]);
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
       m = mnew;
     }
-    if (ok) ok = mbar_wait(&bars->pv_done[h][(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
-    if (ok) {
-      // merge the two halves of the row: M = max(m_0, m_1), a_h = 2^(m_h - M),
-      // L = a_0 l_0 + a_1 l_1, O = a_0 O_0 + a_1 O_1; each half writes 64 of
-      // the 128 channels, half 0 also (M, L)
-      xchg[h * BM + r] = make_float2(m, l);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->merged);
-      ok = mbar_wait(&bars->merged, 0, abort);
-    }
+    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    // L = l_0 + l_1 + l_2 + l_3 in quarter order; every quarter writes its 32
+    // channels of the partial O, quarter 0 also (m, L)
+    if (ok) reinterpret_cast<float *>(&xl[r])[g] = l;
+    for (; nbar <= T; ++nbar) named_bar_sync(1 + quad, 128);
     if (!ok) {
       report(p.status, SAGE_ERR_TIMEOUT);
     } else {
       tc_fence_after();
-      const float2 h0 = xchg[r], h1 = xchg[BM + r];
-      const float M = fmaxf(h0.x, h1.x);
-      const float a0 = h0.x == -INFINITY ? 0.f : ex2(__fsub_rn(h0.x, M));
-      const float a1 = h1.x == -INFINITY ? 0.f : ex2(__fsub_rn(h1.x, M));
-      float *dst = p.part_o + (int64_t(unit) * BM + r) * kD + 64 * h;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t o0[32], o1[32];
-        tmem_ld32(lane_base + col_o(0) + 64 * h + 32 * c, o0);
-        tmem_ld32(lane_base + col_o(1) + 64 * h + 32 * c, o1);
-        tmem_ld_wait(o0);
-        tmem_ld_wait(o1);
-        if (valid) {
+      uint32_t o[32];
+      tmem_ld32(colO, o);
+      tmem_ld_wait(o);
+      if (valid) {
+        float *dst = p.part_o + (int64_t(unit) * BM + r) * kD + kQuarter * g;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              v[e] = __fadd_rn(__fmul_rn(a0, __uint_as_float(o0[4 * u + e])),
-                               __fmul_rn(a1, __uint_as_float(o1[4 * u + e])));
-            *reinterpret_cast<float4 *>(dst + 32 * c + 4 * u) = make_float4(v[0], v[1], v[2], v[3]);
-          }
-        }
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4 *>(dst + 4 * u) =
+              make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]), __uint_as_float(o[4 * u + 2]),
+                          __uint_as_float(o[4 * u + 3]));
       }
-      if (h == 0) p.part_ml[int64_t(unit) * BM + r] = make_float2(M, __fadd_rn(__fmul_rn(a0, h0.y), __fmul_rn(a1, h1.y)));
+      if (g == 0) {
+        const float4 ls = xl[r];
+        p.part_ml[int64_t(unit) * BM + r] =
+            make_float2(m, __fadd_rn(__fadd_rn(__fadd_rn(ls.x, ls.y), ls.z), ls.w));
+      }
     }
   }
   tc_fence_before();
