@@ -453,6 +453,31 @@ sage_status sage_probe_rates(int kind, int iters, unsigned long long *cycles, fl
  * ---------------------------------------------------------------------- */
 sage_status sage_shard_range(int64_t units, int world, int rank, int64_t *begin, int64_t *end);
 
+/* ------------------------------------------------------------------------
+ * sage_debug_bounds - the bounds record of the debug build.
+ *
+ * Not an operation of the method: a checking aid that stands in for a
+ * memory sanitizer.  The library can be built a second time with
+ * -DSAGE_DEBUG_BOUNDS (the package's build(debug_bounds=True) writes
+ * libsage_gb300_debug.so beside the normal library).  In that build every
+ * global load or store whose index a kernel computes is guarded: when the
+ * index falls outside the tensor it belongs to (per the sizes and layouts
+ * documented above), the access is skipped and the first such site is
+ * recorded on the device; nothing traps.  Accesses made by the TMA engine
+ * are bounds-checked by the hardware and are not instrumented.
+ *
+ * sage_debug_bounds synchronises the current device, stores in *site the
+ * first recorded site since the previous call (0 if none; otherwise kernel
+ * file id * 100000 + source line: 1 quant.cu, 2 prepare.cu, 3 kvcache.cu,
+ * 4 attn_dense.cu, 5 attn_int8kv.cu, 6 check.cu) and clears the records.
+ * In the normal build there are no checks and *site is always 0.
+ * SAGE_ERR_INVALID_ARG for a NULL site, SAGE_ERR_CUDA if the device could
+ * not be read.
+ * sage_debug_bounds_enabled: 1 in the debug build, 0 otherwise (host only).
+ * ---------------------------------------------------------------------- */
+sage_status sage_debug_bounds(int32_t *site);
+int sage_debug_bounds_enabled(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,13 +20,13 @@ import ctypes as C
 import math
 import os
 
-from .build import LIB, build as _build_lib
+from .build import DEBUG_LIB, LIB, build as _build_lib
 
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
     "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
     "sage_attention", "sage_attention_host", "sage_shard_range", "sage_quantize_qkv", "sage_attn_fwd_f16",
-    "Strides", "STATUS",
+    "Strides", "STATUS", "use_debug_bounds", "debug_bounds_site",
 ]
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
@@ -55,6 +55,26 @@ def build(force: bool = False) -> str:
     _lib = None
     lib()
     return path
+
+
+def use_debug_bounds(enable: bool = True) -> str:
+    """Route every entry point to the bounds-checking debug library (built on
+    first use) or back to the normal one; returns the library path."""
+    global LIB, _lib
+    LIB = _build_lib(debug_bounds=True) if enable else _build_lib()
+    _lib = None
+    lib()
+    return LIB
+
+
+def debug_bounds_site() -> int:
+    """First out-of-bounds access site recorded by the debug library since the
+    last call (0: none; always 0 for the normal library); clears the record."""
+    site = C.c_int32(0)
+    code = lib().sage_debug_bounds(C.byref(site))
+    if code != 0:
+        raise SageError(code, "sage_debug_bounds")
+    return int(site.value)
 
 
 def lib():
@@ -114,6 +134,9 @@ def lib():
     L.sage_attn_fwd_f16.restype = i32
     L.sage_attn_fwd_f16.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, Strides,
                                     vp, vp, vp]
+    L.sage_debug_bounds.restype = i32
+    L.sage_debug_bounds.argtypes = [C.POINTER(C.c_int32)]
+    L.sage_debug_bounds_enabled.restype = i32
     L.sage_shard_range.restype = i32
     L.sage_shard_range.argtypes = [i64, i32, i32, C.POINTER(i64), C.POINTER(i64)]
     L.int8kv_cache_write.restype = i32

@@ -121,6 +121,30 @@ const char *sage_status_string(sage_status s) {
 
 int sage_abi_version(void) { return kAbiVersion; }
 
+sage_status sage_debug_bounds(int32_t *site) {
+  if (site == nullptr) return SAGE_ERR_INVALID_ARG;
+  *site = 0;
+#ifdef SAGE_DEBUG_BOUNDS
+  if (cudaDeviceSynchronize() != cudaSuccess) return SAGE_ERR_CUDA;
+  int32_t (*const readers[])() = {bounds_take_quant, bounds_take_prepare, bounds_take_kvcache,
+                                  bounds_take_dense,  bounds_take_int8kv,  bounds_take_check};
+  for (auto rd : readers) {
+    const int32_t v = rd();  // reads and clears that file's record
+    if (v < 0) return SAGE_ERR_CUDA;
+    if (*site == 0) *site = v;
+  }
+#endif
+  return SAGE_OK;
+}
+
+int sage_debug_bounds_enabled(void) {
+#ifdef SAGE_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 size_t sage_quantize_qk_workspace(int B, int H, int Nk) {
   if (B < 1 || H < 1 || Nk < 1) return 0;
   return size_t(B) * H * ceil_div(Nk, kMeanChunk) * kD * sizeof(float) + 16;
@@ -457,6 +481,7 @@ sage_status int8kv_cache_write(const void *k_src, const void *v_src, int src_dty
   a.N = N;
   a.Hkv = Hkv;
   a.pos0 = pos0;
+  a.ncache = Ncache;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
   a.cache_head = cache_head_stride;

@@ -43,6 +43,9 @@
 #include "ptx.cuh"
 
 namespace sg {
+
+SG_BOUNDS_FILE(dense, 4)
+
 namespace dense {
 
 constexpr int BM = 128, BN = 128, NSK = 2, NSV = 2;
@@ -68,7 +71,7 @@ constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
 struct Params {
   const float *q_scales, *k_scales, *v_scales;
-  int H, Nq, Nk, q_block, k_block, nbq, nbk;
+  int H, BH, Nq, Nk, q_block, k_block, nbq, nbk;
   float C;  // fl(sm_scale * log2 e)
   __nv_bfloat16 *out;
   sage_strides os;
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ntile = (q0 + BM < p.Nq) ? 2 : 1;  // second query tile present?
   }
   if (q0 >= p.Nq) return;  // the second tile of a ragged last pair: nothing to do
+  if (!SG_BOUNDS(bh < p.BH && q0 >= 0)) return;
   const int coff = p.Nk - p.Nq;                 // causal offset: row i sees keys <= i + coff
   const int T = p.causal ? (min(q0 + ntile * BM, p.Nq) - 1 + coff) / BN + 1 : ceil_div(p.Nk, BN);
 
@@ -323,16 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t colS = lane_base + col_s(t), colO = lane_base + col_o(t);
       uint8_t *sP = smem + kOffP + t * kPBytes + r * 128;
       const uint32_t sw = r & 7;
-      const float sq = valid ? p.q_scales[bh * p.nbq + row / p.q_block] : 0.f;
+      const float sq = (valid && SG_BOUNDS(row / p.q_block < p.nbq)) ? p.q_scales[bh * p.nbq + row / p.q_block] : 0.f;
       const float *skp = p.k_scales + bh * p.nbk;
       float m = -INFINITY, l = 0.f;  // l sums 448 * p
       bool ok = true;
       // dequantisation multipliers t = fl(fl(sq * sk) * C) of a tile's key blocks
       auto tile_t = [&](int j, float &lo, float &hi) {
         if (p.k_block == 128) {
-          lo = hi = __fmul_rn(__fmul_rn(sq, skp[j]), p.C);
+          lo = hi = SG_BOUNDS(j < p.nbk) ? __fmul_rn(__fmul_rn(sq, skp[j]), p.C) : 0.f;
         } else {
-          lo = __fmul_rn(__fmul_rn(sq, skp[2 * j]), p.C);
+          lo = SG_BOUNDS(2 * j < p.nbk) ? __fmul_rn(__fmul_rn(sq, skp[2 * j]), p.C) : 0.f;
           hi = (2 * j + 1 < p.nbk) ? __fmul_rn(__fmul_rn(sq, skp[2 * j + 1]), p.C) : 0.f;
         }
       };
@@ -352,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait(S);
-        if (p.s_dump != nullptr) {  // diagnostic copy of the exact integer scores
+        if (p.s_dump != nullptr && SG_BOUNDS(q0 + t * BM + r < p.nq_pad && j * BN + BN <= p.nk_pad)) {
+          // diagnostic copy of the exact integer scores
           int32_t *d = p.s_dump + (int64_t(bh) * p.nq_pad + (q0 + t * BM + r)) * p.nk_pad + j * BN;
 #pragma unroll
           for (int i = 0; i < 128; i += 4)
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(y0, y1);
             packed[i >> 1] = *reinterpret_cast<const uint32_t *>(&b2);
           }
-          if (valid) {
+          if (valid && SG_BOUNDS(row < p.Nq && bh < p.BH)) {
 #pragma unroll
             for (int u = 0; u < 4; ++u)
               *reinterpret_cast<uint4 *>(dst + 32 * c + 8 * u) =
@@ -531,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // log-sum-exp in the natural base: l sums 448 * 2^(s - m)
-        if (p.lse != nullptr && valid)
+        if (p.lse != nullptr && valid && SG_BOUNDS(row < p.Nq && bh < p.BH))
           p.lse[int64_t(bh) * p.Nq + row] = (m + (log2f(l) - kLog2_448)) * 0.6931471805599453f;
       }
     }
@@ -612,6 +617,7 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.k_scales = a.k_scales;
   p.v_scales = a.v_scales;
   p.H = a.H;
+  p.BH = BH;
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.q_block = a.q_block;

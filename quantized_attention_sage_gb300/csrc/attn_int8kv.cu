@@ -42,6 +42,9 @@
 #include "ptx.cuh"
 
 namespace sg {
+
+SG_BOUNDS_FILE(int8kv, 5)
+
 namespace kv {
 
 constexpr int BM = 128, BN = 128, NSK = 3, NSV = 3;
@@ -166,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T <= 0) {
     // empty key range: record an empty partial for the combine
-    if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4) {
+    if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 &&
+        SG_BOUNDS(unit < int(gridDim.x * gridDim.y * gridDim.z))) {
       const int r = (warp & 3) * 32 + lane;
       p.part_ml[int64_t(unit) * BM + r] = make_float2(-INFINITY, 0.f);
     }
@@ -487,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t o[32];
       tmem_ld32(colO, o);
       tmem_ld_wait(o);
-      if (valid) {
+      const bool unit_ok = SG_BOUNDS(unit < int(gridDim.x * gridDim.y * gridDim.z) && r < BM);
+      if (valid && unit_ok) {
         float *dst = p.part_o + (int64_t(unit) * BM + r) * kD + kQuarter * g;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]), __uint_as_float(o[4 * u + 2]),
                           __uint_as_float(o[4 * u + 3]));
       }
-      if (g == 0) {
+      if (g == 0 && unit_ok) {
         const float4 ls = xl[r];
         p.part_ml[int64_t(unit) * BM + r] =
             make_float2(m, __fadd_rn(__fadd_rn(__fadd_rn(ls.x, ls.y), ls.z), ls.w));
@@ -546,9 +551,11 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
       const __nv_bfloat162 t = __floats2bfloat162_rn(float(b[2 * u]), float(b[2 * u + 1]));
       o[u] = *reinterpret_cast<const uint32_t *>(&t);
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(kimg + (int64_t(g) * Npad + gk) * kD + c16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    if (SG_BOUNDS(gk < Npad && g < int(gridDim.y) && c16 + 16 <= kD)) {
+      uint4 *dst = reinterpret_cast<uint4 *>(kimg + (int64_t(g) * Npad + gk) * kD + c16);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
   }
   // V: the int8 tile lands key-major in shared memory (16-byte loads and
   // stores); each thread then reads one 4-code word of 8 consecutive keys
@@ -595,7 +602,8 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
 #pragma unroll
   for (int rep = 0; rep < 8; ++rep) {
     const int ch = rep * 16 + (threadIdx.x >> 4), q = threadIdx.x & 15;
-    *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + q * 8) = vt[ch][q ^ ((ch >> 2) & 15)];
+    if (SG_BOUNDS(ch < kD && key0 + q * 8 + 8 <= Npad && g < int(gridDim.y)))
+      *reinterpret_cast<uint4 *>(vtimg + (int64_t(g) * kD + ch) * Npad + key0 + q * 8) = vt[ch][q ^ ((ch >> 2) & 15)];
   }
   if (threadIdx.x < BN) {
     const int gk = key0 + threadIdx.x;
@@ -604,8 +612,10 @@ __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restri
       ktv = __fmul_rn(__half2float(ks[g * sc_hs + gk]), C);
       vsv = __half2float(vs[g * sc_hs + gk]);
     }
-    kt[int64_t(g) * Npad + gk] = ktv;
-    vsf[int64_t(g) * Npad + gk] = vsv;
+    if (SG_BOUNDS(gk < Npad && g < int(gridDim.y))) {
+      kt[int64_t(g) * Npad + gk] = ktv;
+      vsf[int64_t(g) * Npad + gk] = vsv;
+    }
     float mx = fabsf(vsv);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -630,6 +640,7 @@ __global__ void __launch_bounds__(256) int8kv_combine_kernel(const float *__rest
   const int g = h / G, hl = h - g * G;
   const int qtile = qi / QT, r = (qi - qtile * QT) * G + hl;
   const int64_t unit0 = (int64_t(g) * nqt + qtile) * nsplit;
+  if (!SG_BOUNDS(qtile < nqt && r < BM && g * G + hl < Hq)) return;
   float M = -INFINITY;
   for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_ml[(unit0 + s) * BM + r].x);
   float L = 0.f;

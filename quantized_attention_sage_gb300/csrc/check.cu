@@ -14,6 +14,8 @@
 
 namespace sg {
 
+SG_BOUNDS_FILE(check, 6)
+
 __global__ void __launch_bounds__(256) conversion_check_kernel(const float *__restrict__ x, int64_t npairs,
                                                                uint8_t *__restrict__ e4m3, int8_t *__restrict__ i8,
                                                                uint16_t *__restrict__ bf16,

@@ -17,6 +17,45 @@ constexpr int kTile = 128;       // keys per softmax tile
 
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Bounds checks of the debug build (compiled with -DSAGE_DEBUG_BOUNDS, the
+// stand-in for a memory sanitizer): SG_BOUNDS(cond) guards a global memory
+// access whose index was computed in the kernel.  When cond is false the
+// access is skipped and the first such site (file id * 100000 + source line)
+// is recorded in a device word of the kernel's file; sage_debug_bounds reads
+// and clears the words of all files.  Nothing traps.  In the normal build
+// SG_BOUNDS(cond) is `true` and costs nothing.  Each kernel file names its id
+// with SG_BOUNDS_FILE(name, id) at namespace sg scope.
+#ifdef SAGE_DEBUG_BOUNDS
+__device__ __forceinline__ bool bounds_check(bool ok, int32_t *word, int32_t site) {
+  if (!ok) atomicCAS(word, 0, site);
+  return ok;
+}
+#define SG_BOUNDS_FILE(name, id)                                             \
+  namespace {                                                                \
+  __device__ int32_t g_bounds_site;                                          \
+  constexpr int32_t kBoundsFile = (id);                                      \
+  }                                                                          \
+  int32_t bounds_take_##name() {                                             \
+    int32_t v = 0;                                                           \
+    const int32_t z = 0;                                                     \
+    if (cudaMemcpyFromSymbol(&v, g_bounds_site, sizeof(v)) != cudaSuccess) v = -1; \
+    cudaMemcpyToSymbol(g_bounds_site, &z, sizeof(z));                        \
+    return v;                                                                \
+  }
+#define SG_BOUNDS(cond) (::sg::bounds_check((cond), &g_bounds_site, kBoundsFile * 100000 + __LINE__))
+#else
+#define SG_BOUNDS_FILE(name, id) \
+  int32_t bounds_take_##name() { return 0; }
+#define SG_BOUNDS(cond) true
+#endif
+// the per-file readers (sage_debug_bounds calls them in file-id order)
+int32_t bounds_take_quant();
+int32_t bounds_take_prepare();
+int32_t bounds_take_kvcache();
+int32_t bounds_take_dense();
+int32_t bounds_take_int8kv();
+int32_t bounds_take_check();
+
 // SM count of the current device (queried per call: a process may drive GPUs
 // of different sizes).
 int current_sm_count();
@@ -125,7 +164,7 @@ struct CacheWriteArgs {
   const void *k_src, *v_src;  // [N tokens][Hkv heads][128], bf16 or fp32
   int64_t src_tok, src_head;  // element strides
   bool f32;
-  int N, Hkv, pos0;
+  int N, Hkv, pos0, ncache;
   int8_t *k_cache, *v_cache;  // [Hkv][Ncache][128]
   int64_t cache_head;         // element stride between heads
   void *k_scale, *v_scale;    // fp16 [Hkv][Ncache]

@@ -26,6 +26,9 @@
 #include "ptx.cuh"
 
 namespace sg {
+
+SG_BOUNDS_FILE(kvcache, 3)
+
 namespace kvc {
 
 template <bool kF32>
@@ -92,6 +95,7 @@ __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteArgs a) {
   if (p >= pend) return;
   int t = int(p / a.Hkv), h = int(p - int64_t(t) * a.Hkv);
   for (; p < pend; ++p) {
+    if (!SG_BOUNDS(t < a.N && h < a.Hkv && int64_t(a.pos0) + t < a.ncache)) return;
     const int64_t off = int64_t(t) * a.src_tok + int64_t(h) * a.src_head + 4 * lane;
     float xk[4], xv[4];
     load_row<kF32>(a.k_src, off, xk);
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
   // raw source bytes of a row slice: 2 x 16 bytes (bf16) or 4 x 16 bytes (fp32)
   constexpr int kVec = kF32 ? 4 : 2;
   auto load = [&](int64_t pp, int tt, int hh, uint4 (&r)[kVec]) {
-    if (pp < P) {
+    if (pp < P && SG_BOUNDS(tt < a.N && hh < a.Hkv)) {
       const int64_t off = int64_t(tt) * a.src_tok + int64_t(hh) * a.src_head + 16 * l8;
       const uint4 *s4 = kF32 ? reinterpret_cast<const uint4 *>(static_cast<const float *>(src) + off)
                              : reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
         for (int k4 = 0; k4 < 4; ++k4) packed[k4] = encode4(k4, std::false_type{});
       }
     }
-    if (live) {
+    if (live && SG_BOUNDS(tc < a.N && hcur < a.Hkv && int64_t(a.pos0) + tc < a.ncache)) {
       const int64_t pos = int64_t(a.pos0) + tc;
       *reinterpret_cast<uint4 *>(cache + int64_t(hcur) * a.cache_head + pos * kD + 16 * l8) =
           make_uint4(packed[0], packed[1], packed[2], packed[3]);

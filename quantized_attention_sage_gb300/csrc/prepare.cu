@@ -27,6 +27,9 @@
 #include "ptx.cuh"
 
 namespace sg {
+
+SG_BOUNDS_FILE(prepare, 2)
+
 namespace prep {
 
 // 1. channel sums of K (z = 0) or maxima of |V| (z = 1) over chunks of 256
@@ -44,6 +47,7 @@ __global__ void __launch_bounds__(64) prep_reduce_kernel(const __nv_bfloat16 *__
   const __nv_bfloat16 *base = (isv ? v : k) + b * s.b + h * s.h + 2 * c2;
   const int t0 = chunk * kMeanChunk;
   const int t1 = min(t0 + kMeanChunk, N);
+  if (!SG_BOUNDS(chunk < nchunks && t0 < N && 2 * c2 + 1 < kD)) return;
   float a0 = 0.f, a1 = 0.f;
   auto take = [&](const __nv_bfloat162 w) {
     const float2 f = __bfloat1622float2(w);
@@ -66,7 +70,9 @@ __global__ void __launch_bounds__(64) prep_reduce_kernel(const __nv_bfloat16 *__
   }
   for (; t < t1; ++t) take(*reinterpret_cast<const __nv_bfloat162 *>(base + int64_t(t) * s.n));
   float *part = isv ? part_v : part_k;
-  *reinterpret_cast<float2 *>(part + (int64_t(bh) * nchunks + chunk) * kD + 2 * c2) = make_float2(a0, a1);
+  const int64_t off = (int64_t(bh) * nchunks + chunk) * kD + 2 * c2;
+  if (SG_BOUNDS(off + 2 <= int64_t(gridDim.y) * nchunks * kD))
+    *reinterpret_cast<float2 *>(part + off) = make_float2(a0, a1);
 }
 
 // 2. per head: K mean = (chunk sums added in ascending order) / N (y = 0);
@@ -89,6 +95,7 @@ __global__ void __launch_bounds__(128) prep_finalize_kernel(const float *__restr
     for (int u = 0; u < 16; ++u) acc = isv ? fmaxf(acc, w[u]) : __fadd_rn(acc, w[u]);
   }
   for (; i < nchunks; ++i) acc = isv ? fmaxf(acc, p[int64_t(i) * kD]) : __fadd_rn(acc, p[int64_t(i) * kD]);
+  if (!SG_BOUNDS(c < kD && bh < int(gridDim.x))) return;
   if (isv) {
     v_scales[bh * kD + c] = __fdiv_rn(acc, 448.f);
     v_inv[bh * kD + c] = acc > 0.f ? __fdiv_rn(448.f, acc) : 0.f;
@@ -132,7 +139,9 @@ __device__ __forceinline__ void encode_qk_block(const __nv_bfloat16 *__restrict_
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int row = (threadIdx.x >> 4) + 16 * i;
-    raw[i] = row < nt ? *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * sn + col) : make_uint4(0, 0, 0, 0);
+    raw[i] = (row < nt && SG_BOUNDS(t0 + row < N && col + 8 <= kD))
+                 ? *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * sn + col)
+                 : make_uint4(0, 0, 0, 0);
   }
   const bool smooth = mean != nullptr;
   auto value = [&](const uint4 &w, int j) -> float {
@@ -157,11 +166,11 @@ __device__ __forceinline__ void encode_qk_block(const __nv_bfloat16 *__restrict_
 #pragma unroll
   for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
   const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
-  if (threadIdx.x == 0) scale_out[blk] = __fdiv_rn(amax, 127.f);
+  if (threadIdx.x == 0 && SG_BOUNDS(t0 < N)) scale_out[blk] = __fdiv_rn(amax, 127.f);
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int row = (threadIdx.x >> 4) + 16 * i;
-    if (row >= nt) continue;
+    if (row >= nt || !SG_BOUNDS(t0 + row < N && col + 8 <= kD)) continue;
     const int64_t off = int64_t(t0 + row) * kD + col;
     if (kImages) {
       // rint (ties to even, as the int8 path's conversion) and the clamp in
@@ -236,7 +245,8 @@ __device__ __forceinline__ void encode_v_tile(const __nv_bfloat16 *__restrict__ 
     o.y = tile[ch * 32 + ((4 * k16 + 1) ^ sw)];
     o.z = tile[ch * 32 + ((4 * k16 + 2) ^ sw)];
     o.w = tile[ch * 32 + ((4 * k16 + 3) ^ sw)];
-    *reinterpret_cast<uint4 *>(dst + int64_t(ch) * Nk_pad + k16 * 16) = o;
+    if (SG_BOUNDS(ch < kD && kt * kTile + k16 * 16 + 16 <= Nk_pad))
+      *reinterpret_cast<uint4 *>(dst + int64_t(ch) * Nk_pad + k16 * 16) = o;
   }
 }
 

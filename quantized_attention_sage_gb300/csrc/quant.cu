@@ -17,6 +17,8 @@
 
 namespace sg {
 
+SG_BOUNDS_FILE(quant, 1)
+
 // -------------------------------------------------------------------------
 // K1: channel sums of K over chunks of 256 tokens, ascending token order.
 // (Also serves V: with kMax it takes channel maxima of |V| instead.)
@@ -32,6 +34,7 @@ __global__ void __launch_bounds__(64) chunk_reduce_kernel(const __nv_bfloat16 *_
   const __nv_bfloat16 *base = x + b * sb + h * sh + 2 * c2;
   const int t0 = chunk * kMeanChunk;
   const int t1 = min(t0 + kMeanChunk, N);
+  if (!SG_BOUNDS(chunk < nchunks && t0 < N && 2 * c2 + 1 < kD)) return;
   float a0 = 0.f, a1 = 0.f;
   int t = t0;
   // 32 rows of loads in flight per round (the additions stay in ascending
@@ -63,7 +66,9 @@ __global__ void __launch_bounds__(64) chunk_reduce_kernel(const __nv_bfloat16 *_
       a1 = __fadd_rn(a1, f.y);
     }
   }
-  *reinterpret_cast<float2 *>(partial + (int64_t(bh) * nchunks + chunk) * kD + 2 * c2) = make_float2(a0, a1);
+  const int64_t off = (int64_t(bh) * nchunks + chunk) * kD + 2 * c2;
+  if (SG_BOUNDS(off + 2 <= int64_t(gridDim.y) * nchunks * kD))
+    *reinterpret_cast<float2 *>(partial + off) = make_float2(a0, a1);
 }
 
 // K1b: mean = (chunk sums added in ascending order) / Nk.  grid B*H, 128 threads.
@@ -82,7 +87,7 @@ __global__ void __launch_bounds__(128) k_mean_finalize_kernel(const float *__res
     for (int u = 0; u < 16; ++u) tot = __fadd_rn(tot, v[u]);
   }
   for (; i < nchunks; ++i) tot = __fadd_rn(tot, p[int64_t(i) * kD]);
-  mean[bh * kD + c] = __fdiv_rn(tot, float(Nk));
+  if (SG_BOUNDS(c < kD && bh < int(gridDim.x))) mean[bh * kD + c] = __fdiv_rn(tot, float(Nk));
 }
 
 // -------------------------------------------------------------------------
@@ -128,8 +133,9 @@ __global__ void __launch_bounds__(256, 4) quant_qk_kernel(const QKQuantArgs a) {
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int row = (threadIdx.x >> 4) + 16 * i;
-    raw[i] = row < nt ? *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * s.n + col)
-                      : make_uint4(0u, 0u, 0u, 0u);
+    raw[i] = (row < nt && SG_BOUNDS(t0 + row < N && col + 8 <= kD))
+                 ? *reinterpret_cast<const uint4 *>(src + int64_t(t0 + row) * s.n + col)
+                 : make_uint4(0u, 0u, 0u, 0u);
   }
   auto value = [&](const uint4 &w, int j) -> float {
     const uint32_t word = j < 2 ? w.x : j < 4 ? w.y : j < 6 ? w.z : w.w;
@@ -156,7 +162,8 @@ __global__ void __launch_bounds__(256, 4) quant_qk_kernel(const QKQuantArgs a) {
   const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
   if (threadIdx.x == 0) {
     float *scales = isk ? a.k_scales : a.q_scales;
-    scales[bh * (isk ? a.nbk : a.nbq) + blk] = __fdiv_rn(amax, 127.f);
+    if (SG_BOUNDS(blk < (isk ? a.nbk : a.nbq) && t0 < N))
+      scales[bh * (isk ? a.nbk : a.nbq) + blk] = __fdiv_rn(amax, 127.f);
   }
   int8_t *dst = (isk ? a.k_codes : a.q_codes) + (int64_t(bh) * N + t0) * kD;
 #pragma unroll
@@ -170,7 +177,8 @@ __global__ void __launch_bounds__(256, 4) quant_qk_kernel(const QKQuantArgs a) {
         c = max(-127, min(127, c));
         w[j >> 2] |= (uint32_t(c) & 0xFFu) << (8 * (j & 3));
       }
-      *reinterpret_cast<uint2 *>(dst + int64_t(row) * kD + col) = make_uint2(w[0], w[1]);
+      if (SG_BOUNDS(t0 + row < N && col + 8 <= kD))
+        *reinterpret_cast<uint2 *>(dst + int64_t(row) * kD + col) = make_uint2(w[0], w[1]);
     }
   }
 }
@@ -192,8 +200,10 @@ __global__ void __launch_bounds__(128) v_finalize_kernel(const float *__restrict
     for (int u = 0; u < 16; ++u) amax = fmaxf(amax, v[u]);
   }
   for (; i < nchunks; ++i) amax = fmaxf(amax, p[int64_t(i) * kD]);
-  v_scales[bh * kD + c] = __fdiv_rn(amax, 448.f);
-  inv[bh * kD + c] = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+  if (SG_BOUNDS(c < kD && bh < int(gridDim.x))) {
+    v_scales[bh * kD + c] = __fdiv_rn(amax, 448.f);
+    inv[bh * kD + c] = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
+  }
 }
 
 // -------------------------------------------------------------------------
@@ -226,7 +236,7 @@ __global__ void __launch_bounds__(256) v_encode_kernel(const __nv_bfloat16 *__re
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int tok = kt * kTile + quad * 4 + r;
-      if (tok < Nk) {
+      if (tok < Nk && SG_BOUNDS(cg * 8 + 8 <= kD)) {
         const uint4 raw = *reinterpret_cast<const uint4 *>(src + int64_t(tok) * vs.n + cg * 8);
         const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
 #pragma unroll
@@ -256,7 +266,8 @@ __global__ void __launch_bounds__(256) v_encode_kernel(const __nv_bfloat16 *__re
     o.y = tile[ch * 32 + ((4 * k16 + 1) ^ sw)];
     o.z = tile[ch * 32 + ((4 * k16 + 2) ^ sw)];
     o.w = tile[ch * 32 + ((4 * k16 + 3) ^ sw)];
-    *reinterpret_cast<uint4 *>(dst + int64_t(ch) * Nk_pad + k16 * 16) = o;
+    if (SG_BOUNDS(ch < kD && kt * kTile + k16 * 16 + 16 <= Nk_pad))
+      *reinterpret_cast<uint4 *>(dst + int64_t(ch) * Nk_pad + k16 * 16) = o;
   }
 }
 
