@@ -71,7 +71,7 @@ constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 
 struct Params {
   const float *q_scales, *k_scales, *v_scales;
-  int H, BH, Nq, Nk, q_block, k_block, nbq, nbk;
+  int H, Nq, Nk, q_block, k_block, nbq, nbk;
   float C;  // fl(sm_scale * log2 e)
   __nv_bfloat16 *out;
   sage_strides os;
@@ -84,6 +84,9 @@ struct Params {
   int fault;         // test hook: 1 = the producer issues no loads; 2 = only Q and the first K tile
   int pairs;         // query-tile pairs per head
   int n_pairs;       // 1-D grid: the first n_pairs CTAs take pairs, the rest single tiles; -1: 2-D grid
+#ifdef SAGE_DEBUG_BOUNDS
+  int BH;  // B * H, for the bounds checks of the debug build
+#endif
 };
 
 struct Bars {
@@ -617,7 +620,9 @@ cudaError_t launch_attn_dense(const DenseArgs &a, cudaStream_t st) {
   p.k_scales = a.k_scales;
   p.v_scales = a.v_scales;
   p.H = a.H;
+#ifdef SAGE_DEBUG_BOUNDS
   p.BH = BH;
+#endif
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.q_block = a.q_block;
