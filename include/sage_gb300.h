@@ -369,6 +369,30 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
                                int32_t *status_dev, void *stream);
 
 /* ------------------------------------------------------------------------
+ * int8kv_prompt_attn_fault_test - exercises the failure detection of
+ * int8kv_prompt_attn: the same launch, except that the kernel's load warp
+ * stops early, so the other warps' bounded waits run out after
+ * wait_limit_ns.
+ *   mode 1: the load warp issues no copy at all;
+ *   mode 2: it loads the query tile and the first two key tiles, then
+ *           stops, so copies and Q.K^T MMAs are issued before the waits give
+ *           up and must complete before the kernel frees its memory.
+ * The kernel sets *status_dev to SAGE_ERR_TIMEOUT, lets every warp pass the
+ * barriers its group shares (they cannot time out), waits for what was
+ * issued, frees its tensor memory and returns; nothing faults, traps or
+ * hangs and the CUDA context stays usable.  The output is not meaningful.
+ * status_dev must not be NULL; wait_limit_ns > 0; mode 1 or 2, else
+ * SAGE_ERR_INVALID_ARG.  Other arguments as int8kv_prompt_attn.
+ * ---------------------------------------------------------------------- */
+sage_status int8kv_prompt_attn_fault_test(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
+                                          const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
+                                          const void *v_scale_f16, int64_t kv_head_stride,
+                                          int64_t scale_head_stride, int Nq, int q_pos0, int Nk, int Hq, int Hkv,
+                                          int d, float sm_scale, void *out_bf16, int64_t o_tok_stride,
+                                          int64_t o_head_stride, void *workspace, size_t workspace_bytes,
+                                          int32_t *status_dev, uint64_t wait_limit_ns, int mode, void *stream);
+
+/* ------------------------------------------------------------------------
  * int8kv_cache_write - quantizes N new K and V rows per kv head into the
  * int8 KV cache read by int8kv_prompt_attn, at cache positions
  * pos0 .. pos0+N-1.  Page: "Strata PR #2092" (an int8 K/V cache with

@@ -24,7 +24,7 @@ from .build import DEBUG_LIB, LIB, build as _build_lib
 
 __all__ = [
     "SageError", "build", "lib", "sage_quantize_qk", "sage_quantize_v", "sage_attn_fwd",
-    "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_cache_write",
+    "sage_attn_fwd_scores_dump", "sage_attn_fwd_fault_test", "int8kv_prompt_attn", "int8kv_prompt_attn_fault_test", "int8kv_cache_write",
     "sage_attention", "sage_attention_host", "sage_shard_range", "sage_quantize_qkv", "sage_attn_fwd_f16",
     "Strides", "STATUS", "use_debug_bounds", "debug_bounds_site",
 ]
@@ -144,6 +144,9 @@ def lib():
                                      vp, vp]
     L.int8kv_prompt_attn_workspace.restype = sz
     L.int8kv_prompt_attn_workspace.argtypes = [i32, i32, i32, i32]
+    L.int8kv_prompt_attn_fault_test.restype = i32
+    L.int8kv_prompt_attn_fault_test.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32,
+                                                i32, f32, vp, i64, i64, vp, sz, vp, C.c_uint64, i32, vp]
     L.int8kv_prompt_attn.restype = i32
     L.int8kv_prompt_attn.argtypes = [vp, i64, i64, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32,
                                      i32, f32, vp, i64, i64, vp, sz, vp, vp]
@@ -476,7 +479,7 @@ def sage_attention_host(q, k, v, out, q_block: int = 64, k_block: int = 64, sm_s
 # ---------------------------------------------------------------------------
 
 def int8kv_prompt_attn(q, k_cache, k_scale, v_cache, v_scale, q_pos0: int, sm_scale: float = 0.0,
-                       out=None, workspace=None, status=None, stream=None):
+                       out=None, workspace=None, status=None, stream=None, _fault=None):
     """Causal prompt attention of q [Nq,Hq,128] bf16 over an int8 cache.
 
     k_cache, v_cache: int8 [Hkv, Nk, 128] (token rows contiguous);
@@ -496,12 +499,28 @@ def int8kv_prompt_attn(q, k_cache, k_scale, v_cache, v_scale, q_pos0: int, sm_sc
     L = lib()
     nbytes = L.int8kv_prompt_attn_workspace(Nq, Hq, Hkv, Nk)
     ws = _workspace(nbytes, dev, workspace)
-    _check(L.int8kv_prompt_attn(_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(k_scale),
-                                _ptr(v_cache), _ptr(v_scale), k_cache.stride(0), k_scale.stride(0), Nq,
-                                int(q_pos0), Nk, Hq, Hkv, D, float(sm_scale), _ptr(out), out.stride(0),
-                                out.stride(1), _ptr(ws), nbytes, _ptr(status), _stream(stream)),
-           "int8kv_prompt_attn")
+    args = (_ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(k_scale), _ptr(v_cache), _ptr(v_scale),
+            k_cache.stride(0), k_scale.stride(0), Nq, int(q_pos0), Nk, Hq, Hkv, D, float(sm_scale), _ptr(out),
+            out.stride(0), out.stride(1), _ptr(ws), nbytes, _ptr(status))
+    if _fault is not None:  # (wait_limit_ns, mode): int8kv_prompt_attn_fault_test
+        _check(L.int8kv_prompt_attn_fault_test(*args, int(_fault[0]), int(_fault[1]), _stream(stream)),
+               "int8kv_prompt_attn_fault_test")
+        return out
+    _check(L.int8kv_prompt_attn(*args, _stream(stream)), "int8kv_prompt_attn")
     return out
+
+
+def int8kv_prompt_attn_fault_test(q, k_cache, k_scale, v_cache, v_scale, q_pos0: int, wait_limit_ns: int,
+                                  mode: int, stream=None) -> int:
+    """int8kv_prompt_attn with its load warp stopped early (mode 1: no copy; mode 2: Q and two K
+    tiles), so the bounded waits run out after wait_limit_ns; returns the device status word
+    (SAGE_ERR_TIMEOUT expected).  Test hook only."""
+    torch = _torch()
+    status = torch.zeros(1, dtype=torch.int32, device=q.device)
+    int8kv_prompt_attn(q, k_cache, k_scale, v_cache, v_scale, q_pos0, status=status, stream=stream,
+                       _fault=(wait_limit_ns, mode))
+    torch.cuda.synchronize(q.device)
+    return int(status.item())
 
 
 def int8kv_cache_write(k, v, k_cache, k_scale, v_cache, v_scale, pos0: int, status=None, stream=None):

@@ -384,12 +384,15 @@ size_t int8kv_prompt_attn_workspace(int Nq, int Hq, int Hkv, int Nk) {
   return int8kv_workspace_bytes(Nq, Hq, Hkv, Nk);
 }
 
-sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
-                               const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
-                               const void *v_scale_f16, int64_t kv_head_stride, int64_t scale_head_stride, int Nq,
-                               int q_pos0, int Nk, int Hq, int Hkv, int d, float sm_scale, void *out_bf16,
-                               int64_t o_tok_stride, int64_t o_head_stride, void *workspace,
-                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+}  // extern "C"
+
+namespace {
+sage_status int8kv_impl(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride, const int8_t *k_cache,
+                        const void *k_scale_f16, const int8_t *v_cache, const void *v_scale_f16,
+                        int64_t kv_head_stride, int64_t scale_head_stride, int Nq, int q_pos0, int Nk, int Hq,
+                        int Hkv, int d, float sm_scale, void *out_bf16, int64_t o_tok_stride,
+                        int64_t o_head_stride, void *workspace, size_t workspace_bytes, int32_t *status_dev,
+                        void *stream, uint64_t wait_ns, int fault) {
   if (d != kD) return SAGE_ERR_UNSUPPORTED;
   if (Nq < 1 || Nk < 1 || Hq < 1 || Hkv < 1 || q_pos0 < 0 || int64_t(q_pos0) + Nq > Nk) return SAGE_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return SAGE_ERR_INVALID_ARG;
@@ -423,7 +426,36 @@ sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t
   a.o_head = o_head_stride;
   a.workspace = workspace;
   a.status = status_dev;
+  a.wait_ns = wait_ns;
+  a.fault = fault;
   return from_cuda(launch_int8kv(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+sage_status int8kv_prompt_attn(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
+                               const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
+                               const void *v_scale_f16, int64_t kv_head_stride, int64_t scale_head_stride, int Nq,
+                               int q_pos0, int Nk, int Hq, int Hkv, int d, float sm_scale, void *out_bf16,
+                               int64_t o_tok_stride, int64_t o_head_stride, void *workspace,
+                               size_t workspace_bytes, int32_t *status_dev, void *stream) {
+  return int8kv_impl(q_bf16, q_tok_stride, q_head_stride, k_cache, k_scale_f16, v_cache, v_scale_f16, kv_head_stride,
+                     scale_head_stride, Nq, q_pos0, Nk, Hq, Hkv, d, sm_scale, out_bf16, o_tok_stride, o_head_stride,
+                     workspace, workspace_bytes, status_dev, stream, 2000000000ull, 0);
+}
+
+sage_status int8kv_prompt_attn_fault_test(const void *q_bf16, int64_t q_tok_stride, int64_t q_head_stride,
+                                          const int8_t *k_cache, const void *k_scale_f16, const int8_t *v_cache,
+                                          const void *v_scale_f16, int64_t kv_head_stride,
+                                          int64_t scale_head_stride, int Nq, int q_pos0, int Nk, int Hq, int Hkv,
+                                          int d, float sm_scale, void *out_bf16, int64_t o_tok_stride,
+                                          int64_t o_head_stride, void *workspace, size_t workspace_bytes,
+                                          int32_t *status_dev, uint64_t wait_limit_ns, int mode, void *stream) {
+  if (status_dev == nullptr || wait_limit_ns == 0 || (mode != 1 && mode != 2)) return SAGE_ERR_INVALID_ARG;
+  return int8kv_impl(q_bf16, q_tok_stride, q_head_stride, k_cache, k_scale_f16, v_cache, v_scale_f16, kv_head_stride,
+                     scale_head_stride, Nq, q_pos0, Nk, Hq, Hkv, d, sm_scale, out_bf16, o_tok_stride, o_head_stride,
+                     workspace, workspace_bytes, status_dev, stream, wait_limit_ns, mode);
 }
 
 sage_status sage_conversion_check(const float *x, int64_t n, uint8_t *e4m3, int8_t *i8, uint16_t *bf16,

@@ -89,6 +89,8 @@ struct Params {
   float *part_o;               // [units][128][128]
   float2 *part_ml;             // [units][128] (m, l)
   int32_t *status;
+  uint64_t wait_ns;  // limit of every bounded wait
+  int fault;         // test hook: 1 = the producer issues no copy; 2 = only Q and the first two K tiles
 };
 
 struct Bars {
@@ -177,7 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (converged warp)
     const bool leader = elect_one();
-    if (leader) {
+    // Test hooks: fault == 1 issues nothing; fault == 2 loads Q and the first
+    // two K tiles and stops.  Either way the consumers' bounded waits run out
+    // and the kernel reports SAGE_ERR_TIMEOUT.
+    const bool q_issued = p.fault != 1;
+    if (leader && q_issued) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
@@ -189,8 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int nk = 0, nv = 0;  // K and V tiles issued
     auto load_k = [&](int j) -> bool {
       const int s = j % NSK;
-      if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort)) return false;
-      if (j == 2 && !mbar_wait(&bars->q_tmem, 0, abort)) return false;  // stage 2 is the Q tile
+      if (j >= NSK && !mbar_wait(&bars->k_empty[s], ((j / NSK) + 1) & 1, abort, p.wait_ns)) return false;
+      if (j == 2 && !mbar_wait(&bars->q_tmem, 0, abort, p.wait_ns)) return false;  // stage 2 is the Q tile
       if (leader) {
         const int key0 = (tb + j) * BN;
         uint8_t *dst = smem + k_stage(s);
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto load_v = [&](int j) -> bool {
       const int s = j % NSV;
-      if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort)) return false;
+      if (j >= NSV && !mbar_wait(&bars->v_empty[s], ((j / NSV) + 1) & 1, abort, p.wait_ns)) return false;
       if (leader) {
         const int key0 = (tb + j) * BN;
         uint8_t *dst = smem + kOffV + s * kVBytes;
@@ -221,19 +227,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // order of first use: K0, K1, V0, K2, V1, K3, ...; K(j+2) waits for the
     // Q.K^T of tile j-1, one tile earlier than a two-stage ring would
-    bool ok = load_k(0) && (T < 2 || load_k(1));
-    for (int j = 0; ok && j < T; ++j) {
+    bool ok = p.fault == 1 || (load_k(0) && (T < 2 || load_k(1)));
+    for (int j = 0; ok && p.fault == 0 && j < T; ++j) {
       ok = load_v(j);
       if (ok && j + 2 < T) ok = load_k(j + 2);
     }
     // Every copy issued here lands in this CTA's shared memory: wait for the
     // last phase of each barrier it armed before the CTA may exit, also when
     // the consumers gave up and no longer wait for them.
-    bool drained = mbar_drain(&bars->q_full, 0);
+    bool drained = !q_issued || mbar_drain(&bars->q_full, 0, p.wait_ns);
     for (int s = 0; s < NSK; ++s)
-      if (nk > s) drained &= mbar_drain(&bars->k_full[s], ((nk - 1 - s) / NSK) & 1);
+      if (nk > s) drained &= mbar_drain(&bars->k_full[s], ((nk - 1 - s) / NSK) & 1, p.wait_ns);
     for (int s = 0; s < NSV; ++s)
-      if (nv > s) drained &= mbar_drain(&bars->v_full[s], ((nv - 1 - s) / NSV) & 1);
+      if (nv > s) drained &= mbar_drain(&bars->v_full[s], ((nv - 1 - s) / NSV) & 1, p.wait_ns);
     if ((!ok || !drained) && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (converged warp)
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t last_par = 0;
     auto issue_qk = [&](int j) -> bool {
       const int s = j % NSK;
-      if (!mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort)) return false;
+      if (!mbar_wait(&bars->k_full[s], (j / NSK) & 1, abort, p.wait_ns)) return false;
       tc_fence_after();
       const uint32_t sK = smem_u32(smem + k_stage(s));
       if (leader) {
@@ -264,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       last_par = (j >> 1) & 1;
       return true;
     };
-    bool ok = mbar_wait(&bars->q_tmem, 0, abort);
+    bool ok = mbar_wait(&bars->q_tmem, 0, abort, p.wait_ns);
     tc_fence_after();
     ok = ok && issue_qk(0) && (T < 2 || issue_qk(1));
     for (int j = 0; ok && j < T; ++j) {
       const int s = j % NSV, b = j & 1;
-      ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort) && mbar_wait(&bars->p_full[b], (j >> 1) & 1, abort);
+      ok = mbar_wait(&bars->v_full[s], (j / NSV) & 1, abort, p.wait_ns) &&
+           mbar_wait(&bars->p_full[b], (j >> 1) & 1, abort, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
       const uint32_t sV = smem_u32(smem + kOffV + s * kVBytes);
@@ -297,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the MMAs read shared memory and write TMEM: wait for the last commit
     // before the CTA may free either
-    if (last_bar != nullptr && !mbar_drain(last_bar, last_par)) ok = false;
+    if (last_bar != nullptr && !mbar_drain(last_bar, last_par, p.wait_ns)) ok = false;
     if (!ok && leader) report(p.status, SAGE_ERR_TIMEOUT);
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------ softmax of one key quarter
@@ -327,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Q into TMEM: row r's 128 bf16 (two 128-byte swizzled rows of the TMA
       // boxes; 16-byte chunk c of row r sits at chunk c ^ (r & 7)) become 64
       // columns of bf16 pairs, the A-operand layout of Q.K^T
-      ok = mbar_wait(&bars->q_full, 0, abort);
+      ok = mbar_wait(&bars->q_full, 0, abort, p.wait_ns);
       if (ok) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; ok && j < T; ++j) {
       const int b = j & 1;
-      ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort);
+      ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, abort, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
       const uint32_t sa = lane_base + col_s(b) + kQuarter * g;
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kt and vs of this tile arrived with V(j); its slot is reused only
       // after the P.V of tile j, which waits for this warp's p_full
       const int sv = j % NSV;
-      ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort);
+      ok = mbar_wait(&bars->v_full[sv], (j / NSV) & 1, abort, p.wait_ns);
       if (!ok) break;
       const float4 *kt4 = reinterpret_cast<const float4 *>(smem + kOffKt + sv * BN * 4) + kQuarter / 4 * g;
       const float4 *vs4 = reinterpret_cast<const float4 *>(smem + kOffVs + sv * BN * 4) + kQuarter / 4 * g;
@@ -458,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O is stable once the P.V of tile j-1 is complete; this quarter's
       // warps rescale their 32 columns of it when the row max grew
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort);
+        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         uint32_t o[32];
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->p_full[b]);
       m = mnew;
     }
-    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort);
+    if (ok) ok = mbar_wait(&bars->pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, abort, p.wait_ns);
     // L = l_0 + l_1 + l_2 + l_3 in quarter order; every quarter writes its 32
     // channels of the partial O, quarter 0 also (m, L)
     if (ok) reinterpret_cast<float *>(&xl[r])[g] = l;
@@ -759,6 +766,8 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   p.part_o = po;
   p.part_ml = pml;
   p.status = a.status;
+  p.wait_ns = a.wait_ns;
+  p.fault = a.fault;
   static CtxOnce attr_done;
   e = set_smem_attr_once(reinterpret_cast<const void *>(int8kv_attn_kernel), kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;

@@ -155,6 +155,8 @@ struct Int8KVArgs {
   int64_t o_tok, o_head;
   void *workspace;
   int32_t *status;
+  uint64_t wait_ns = 2000000000ull;  // limit of every bounded wait in the kernel
+  int fault = 0;                     // test hook of int8kv_prompt_attn_fault_test
 };
 size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk);
 cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st);

@@ -60,3 +60,53 @@ def test_fault_test_rejects_bad_arguments(cuda_lib):
     rc = L.sage_attn_fwd_fault_test(None, None, None, None, None, None, 1, 1, 128, 128, 128, 64, 64, 0.0,
                                     None, cuda_lib.Strides(0, 0, 0), None, 0, status.data_ptr(), 1000, 3, None)
     assert rc == 1
+
+
+# The int8-KV kernel: its softmax warps also meet at named barriers, which
+# cannot time out; after a bounded wait gives up, every warp must still pass
+# the same number of them.  Mode 2 loads Q and two K tiles, so the Q copy into
+# tensor memory, two Q.K^T MMAs and the first scores are done before the waits
+# for V give up; split-KV (several CTAs per query tile) is on in the larger case.
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("wname", ["tiny_kv_q96_k300", "kv_split_fault"])
+def test_int8kv_bounded_wait_reports_timeout_and_context_survives(cuda_lib, mode, wname):
+    from test_gpu_int8kv import oracle_bf16, run
+    from gpu_helpers import assert_output_close, bf16_to_f64
+    import numpy as np
+
+    w = (synth.int8kv_workload(wname) if wname.startswith("tiny")
+         else synth.Int8KVWorkload(wname, 9, 256, 4096, 32, 8, sub=11))
+    x = synth.int8kv_inputs(w)
+    from kv_helpers import device_cache
+    q, kc, ks, vc, vs = device_cache(cuda_lib, x)
+
+    limit_ns = 20_000_000  # 20 ms
+    t0 = time.perf_counter()
+    status = cuda_lib.int8kv_prompt_attn_fault_test(q, kc, ks, vc, vs, w.q_pos0, limit_ns, mode)
+    elapsed = time.perf_counter() - t0
+    assert status == SAGE_ERR_TIMEOUT
+    assert elapsed < 2.0, elapsed
+    assert cuda_lib.int8kv_prompt_attn_fault_test(q, kc, ks, vc, vs, w.q_pos0, limit_ns, mode) == SAGE_ERR_TIMEOUT
+
+    # the context is still usable: a normal call afterwards matches the oracle
+    host, out = run(cuda_lib, w, x)
+    rng = np.random.default_rng(3)
+    rows = rng.integers(0, w.Nq, 64)
+    heads = rng.integers(0, w.Hq, 64)
+    ref_b, _ = oracle_bf16(w, host, rows, heads)
+    got = bf16_to_f64(out[torch.from_numpy(rows), torch.from_numpy(heads)])
+    assert_output_close(got, ref_b, f"int8kv after timeout, mode {mode}")
+
+
+def test_int8kv_fault_test_rejects_bad_arguments(cuda_lib):
+    L = cuda_lib.lib()
+    rc = L.int8kv_prompt_attn_fault_test(None, 0, 0, None, None, None, None, 0, 0, 1, 0, 1, 1, 1, 128, 0.0, None, 0,
+                                         0, None, 0, None, 1000, 1, None)
+    assert rc == 1  # NULL status word
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = L.int8kv_prompt_attn_fault_test(None, 0, 0, None, None, None, None, 0, 0, 1, 0, 1, 1, 1, 128, 0.0, None, 0,
+                                         0, None, 0, status.data_ptr(), 0, 1, None)
+    assert rc == 1  # zero limit
+    rc = L.int8kv_prompt_attn_fault_test(None, 0, 0, None, None, None, None, 0, 0, 1, 0, 1, 1, 1, 128, 0.0, None, 0,
+                                         0, None, 0, status.data_ptr(), 1000, 3, None)
+    assert rc == 1  # unknown mode
