@@ -355,7 +355,9 @@ sage_status sage_attn_fwd_fault_test(const int8_t *q_codes, const float *q_scale
  *   [Hkv, Nk, 128] with kv_head_stride elements between heads and 128 between
  *   tokens; k_scale_f16, v_scale_f16 fp16 [Hkv, Nk] with scale_head_stride;
  *   out_bf16 [Nq, Hq, 128] with o_tok_stride, o_head_stride.
- * Requires Hq % Hkv == 0, 1 <= Nq, q_pos0 >= 0, q_pos0 + Nq <= Nk.
+ * Requires Hq % Hkv == 0, 1 <= Nq, q_pos0 >= 0, q_pos0 + Nq <= Nk.  Cache
+ * positions q_pos0 + Nq .. Nk - 1 are visible to no query and never read, so
+ * a chunk may attend within a longer, partly filled cache.
  * sm_scale <= 0 selects 1/sqrt(128).  Workspace: at least
  * int8kv_prompt_attn_workspace(Nq, Hq, Hkv, Nk) bytes.
  * ---------------------------------------------------------------------- */

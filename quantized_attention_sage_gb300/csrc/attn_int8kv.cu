@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "internal.h"
@@ -525,8 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Prepare the cache for the tensor cores: bf16 images of the K codes
 // [Hkv][Npad][128], fp16 images of the V codes transposed [Hkv][128][Npad],
-// kt = fl(ks * C) and vs as fp32 [Hkv][Npad] (zero past Nk), and the maximum
-// of vs.  grid (Npad/128, Hkv), 256 threads.
+// kt = fl(ks * C) and vs as fp32 [Hkv][Npad], and the maximum of vs, for the
+// first Nk keys (the visible ones; images and scales are zero from Nk to the
+// end of the last tile).  grid (ceil(Nk / 128), Hkv), 256 threads.
 __global__ void __launch_bounds__(256) int8kv_prep_kernel(const int8_t *__restrict__ kc, const int8_t *__restrict__ vc,
                                                           const __half *__restrict__ ks, const __half *__restrict__ vs,
                                                           int64_t kv_hs, int64_t sc_hs, int Nk, int Npad, float C,
@@ -678,27 +680,32 @@ struct Layout {
   size_t off_kimg, off_vt, off_kt, off_vs, off_vmax, off_po, off_pml, total;
 };
 
-static Layout layout(int Nq, int Hq, int Hkv, int Nk, int sms) {
-  Layout L;
-  L.G = Hq / Hkv;
-  L.QT = BM / L.G;
-  L.nqt = ceil_div(Nq, L.QT);
-  L.Npad = nk_pad(Nk);
-  // split-KV: pick the split count that minimises waves x (tiles per unit + 2)
-  const int tiles = ceil_div(Nk, BN);
-  const int64_t base_units = int64_t(Hkv) * L.nqt;
+// split-KV: the split count that minimises waves x (key tiles per unit + 2)
+static int choose_nsplit(int64_t base_units, int tiles, int sms) {
   double best = 1e300;
-  L.nsplit = 1;
+  int nsplit = 1;
   for (int s = 1; s <= 16 && s <= tiles; ++s) {
     const int64_t units = base_units * s;
     const int64_t waves = (units + sms - 1) / sms;
     const double cost = double(waves) * (double(tiles) / s + 2.0);
     if (cost < best - 1e-9) {
       best = cost;
-      L.nsplit = s;
+      nsplit = s;
     }
   }
-  const int64_t units = base_units * L.nsplit;
+  return nsplit;
+}
+
+// Workspace layout for a cache of Nk tokens (the split partials sized for the
+// split count of the whole cache, an upper bound for any launch on it).
+static Layout layout(int Nq, int Hq, int Hkv, int Nk, int sms) {
+  Layout L;
+  L.G = Hq / Hkv;
+  L.QT = BM / L.G;
+  L.nqt = ceil_div(Nq, L.QT);
+  L.Npad = nk_pad(Nk);
+  L.nsplit = choose_nsplit(int64_t(Hkv) * L.nqt, ceil_div(Nk, BN), sms);
+  const int64_t units = int64_t(Hkv) * L.nqt * L.nsplit;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -724,7 +731,14 @@ size_t int8kv_workspace_bytes(int Nq, int Hq, int Hkv, int Nk) {
 
 cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   using namespace kv;
-  const Layout L = layout(a.Nq, a.Hq, a.Hkv, a.Nk, current_sm_count());
+  const int sms = current_sm_count();
+  const Layout L = layout(a.Nq, a.Hq, a.Hkv, a.Nk, sms);
+  // Keys at positions q_pos0 + Nq and beyond are visible to no query: the
+  // images, the split and the key loop cover only the first nvis keys, and
+  // the rest of the cache is never read.
+  const int nvis = a.q_pos0 + a.Nq;
+  const int tiles_vis = ceil_div(nvis, BN);
+  const int nsplit = std::min(choose_nsplit(int64_t(a.Hkv) * L.nqt, tiles_vis, sms), L.nsplit);
   uint8_t *ws = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(a.workspace) + 255) & ~uintptr_t(255));
   auto *kimg = reinterpret_cast<__nv_bfloat16 *>(ws + L.off_kimg);
   auto *vtimg = reinterpret_cast<__half *>(ws + L.off_vt);
@@ -736,9 +750,9 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   const float C = a.sm_scale * 1.44269504f;
 
   zero_word_kernel<<<1, 1, 0, st>>>(vmax);
-  int8kv_prep_kernel<<<dim3(L.Npad / BN, a.Hkv), 256, 0, st>>>(
+  int8kv_prep_kernel<<<dim3(tiles_vis, a.Hkv), 256, 0, st>>>(
       a.k_cache, a.v_cache, static_cast<const __half *>(a.k_scale), static_cast<const __half *>(a.v_scale),
-      a.kv_head_stride, a.scale_head_stride, a.Nk, L.Npad, C, kimg, vtimg, kt, vsf, vmax);
+      a.kv_head_stride, a.scale_head_stride, nvis, L.Npad, C, kimg, vtimg, kt, vsf, vmax);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -758,7 +772,7 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   p.Hkv = a.Hkv;
   p.G = L.G;
   p.QT = L.QT;
-  p.nsplit = L.nsplit;
+  p.nsplit = nsplit;
   p.Npad = L.Npad;
   p.kt = kt;
   p.vs = vsf;
@@ -771,11 +785,11 @@ cudaError_t launch_int8kv(const Int8KVArgs &a, cudaStream_t st) {
   static CtxOnce attr_done;
   e = set_smem_attr_once(reinterpret_cast<const void *>(int8kv_attn_kernel), kSmemBytes, &attr_done);
   if (e != cudaSuccess) return e;
-  int8kv_attn_kernel<<<dim3(L.nsplit, L.nqt, a.Hkv), kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
+  int8kv_attn_kernel<<<dim3(nsplit, L.nqt, a.Hkv), kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int rows = a.Nq * a.Hq;
-  int8kv_combine_kernel<<<ceil_div(rows, 8), 256, 0, st>>>(po, pml, a.Nq, a.Hq, L.G, L.QT, L.nqt, L.nsplit,
+  int8kv_combine_kernel<<<ceil_div(rows, 8), 256, 0, st>>>(po, pml, a.Nq, a.Hq, L.G, L.QT, L.nqt, nsplit,
                                                           static_cast<__nv_bfloat16 *>(a.out), a.o_tok, a.o_head);
   return cudaGetLastError();
 }

@@ -135,3 +135,36 @@ def test_int8kv_strided_queries_and_output(cuda_lib):
     torch.cuda.synchronize()
     assert torch.equal(ov.view(torch.int16), ref.view(torch.int16))
     assert torch.isnan(big[:, 0].float()).all() and torch.isnan(big[:, w.Hq + 1:].float()).all()
+
+
+def test_int8kv_chunk_inside_a_longer_cache(cuda_lib):
+    """Queries that end before the cache does (q_pos0 + Nq < Nk, e.g. a chunk of a
+    prompt whose later tokens are already cached): every row against the fp64
+    oracle; the positions no query sees are never read (other codes and NaN scales
+    there change no bit); and the result equals the call on the cache cut to the
+    visible keys (same images, split and scaling)."""
+    w = synth.Int8KVWorkload("kv_mid", 9, 70, 3000, 8, 2, sub=13)
+    host, (q, kc, ks, vc, vs) = both_caches(cuda_lib, synth.int8kv_inputs(w))
+    p0 = 900
+    nvis = p0 + w.Nq  # keys 0..969 are visible to some query, 970..2999 to none
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = cuda_lib.int8kv_prompt_attn(q, kc, ks, vc, vs, p0, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    rows, heads = np.meshgrid(np.arange(w.Nq), np.arange(w.Hq), indexing="ij")
+    ref, _ = oracle.int8kv_rows(host["q"], host["k"], host["k_scale"], host["v"], host["v_scale"], p0,
+                                rows.ravel(), heads.ravel())
+    ref_b = oracle.bf16_value(oracle.f32_to_bf16(ref.astype(np.float32)))
+    assert_output_close(bf16_to_f64(out).reshape(-1, 128), ref_b, w.name)
+
+    kc2, vc2, ks2, vs2 = kc.clone(), vc.clone(), ks.clone(), vs.clone()
+    g = torch.Generator(device="cuda").manual_seed(3)
+    kc2[:, nvis:] = torch.randint(-127, 128, kc2[:, nvis:].shape, generator=g, device="cuda", dtype=torch.int8)
+    vc2[:, nvis:] = torch.randint(-127, 128, vc2[:, nvis:].shape, generator=g, device="cuda", dtype=torch.int8)
+    ks2.view(torch.int16)[:, nvis:] = 0x7E00  # fp16 NaN
+    vs2.view(torch.int16)[:, nvis:] = 0x7E00
+    out2 = cuda_lib.int8kv_prompt_attn(q, kc2, ks2, vc2, vs2, p0)
+    out3 = cuda_lib.int8kv_prompt_attn(q, kc[:, :nvis], ks[:, :nvis], vc[:, :nvis], vs[:, :nvis], p0)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(out3.view(torch.int16), out.view(torch.int16))
