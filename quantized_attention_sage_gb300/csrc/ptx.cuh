@@ -394,7 +394,6 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
-// max of three (sm_100+)
 __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
   float2 d;
   asm("{.reg .b64 ra, rb, rd;\n\t"
@@ -404,6 +403,7 @@ __device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+// max of three (sm_100+)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
