@@ -3,10 +3,14 @@
 small and ragged shapes of each entry point must record no out-of-bounds
 site and give outputs bit for bit equal to the normal build's."""
 
+import numpy as np
 import pytest
 import torch
 
 import quantized_attention_sage_gb300 as qas
+import synth
+from gpu_helpers import bf16_dev
+from kv_helpers import device_cache
 
 pytestmark = pytest.mark.gpu
 
@@ -103,3 +107,39 @@ def test_every_kernel_in_bounds_and_equal_to_the_normal_build(cuda_lib):
         if a.dtype in as_int:
             a, b = a.contiguous().view(as_int[a.dtype]), b.contiguous().view(as_int[b.dtype])
         assert torch.equal(a, b), key
+
+
+def test_full_size_workloads_in_bounds_and_equal_to_the_normal_build(cuda_lib):
+    """The benchmark's own launches through the bounds-checking build: the
+    37,810-token, 24-head dense path in one call (fused preparation, then the
+    attention over the images, last-wave single-tile CTAs included) and both
+    int8-KV prompt chunks (split-KV): no out-of-bounds site, same bits."""
+    w = synth.dense_workload("videodit_b1h24n37810")
+    x = synth.dense_inputs(w)
+    q, k, v = bf16_dev(x["q"]), bf16_dev(x["k"]), bf16_dev(x["v"])
+    del x
+    caches = [(wk, device_cache(qas, synth.int8kv_inputs(wk)))
+              for wk in (synth.int8kv_workload("prompt32k_q1024"), synth.int8kv_workload("prompt64k_q512_outliers"))]
+
+    def run_all():
+        res = {"dense": qas.sage_attention(q, k, v, w.block, w.block).clone()}
+        for wk, (qq, kc, ks, vc, vs) in caches:
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            res[wk.name] = qas.int8kv_prompt_attn(qq, kc, ks, vc, vs, wk.q_pos0, status=st).clone()
+            torch.cuda.synchronize()
+            assert st.item() == 0, wk.name
+        return res
+
+    qas.use_debug_bounds(False)
+    normal = run_all()
+    try:
+        qas.use_debug_bounds(True)
+        assert qas.debug_bounds_site() == 0
+        debug = run_all()
+        site = qas.debug_bounds_site()
+        assert site == 0, f"out-of-bounds access recorded at file {site // 100000}, line {site % 100000}"
+    finally:
+        qas.use_debug_bounds(False)
+    for key in normal:
+        assert torch.equal(normal[key].view(torch.int16), debug[key].view(torch.int16)), key
+    assert np.isfinite(normal["dense"].float().cpu().numpy()).all()
