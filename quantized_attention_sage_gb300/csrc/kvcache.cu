@@ -10,17 +10,17 @@
 //           fp16 scale is 0.
 //
 // GB300 design: HBM-bound streaming.  Rows whose source is 16-byte aligned
-// take a wide kernel (8 lanes per row, four rows per warp); others one warp
-// per row, four channels per lane (8- or 16-byte loads, 4-byte code stores: a
-// row is one 128-byte line of the cache), the row maximum by warp shuffles, one division-free code per
-// channel (a multiply by the correctly rounded reciprocal of the scale, with
-// the exact quotient taken only next to a rounding boundary), no 64-bit
-// division in the row loop; one resident grid of 8 blocks of 256 threads per
-// SM.
+// take a wide kernel (8 lanes per row, four rows per warp, rows walked head by
+// head so every address advances by a constant, source slices staged through
+// shared memory with cp.async several steps ahead); others one warp per row,
+// four channels per lane (8- or 16-byte loads, 4-byte code stores: a row is
+// one 128-byte line of the cache).  The row maximum by warp shuffles, one
+// division-free code per channel (a multiply by the correctly rounded
+// reciprocal of the scale, with the exact quotient taken only next to a
+// rounding boundary), no 64-bit division in the row loop; one wave of equal
+// CTAs, as many as fit on the SMs at once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-
-#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -112,58 +112,81 @@ __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteArgs a) {
 }
 
 // Wide variant for 16-byte aligned rows: 8 lanes per row, 16 channels per
-// lane (16-byte loads and code stores), four rows per warp (the K and V rows
-// of two consecutive (token, head) pairs), the row maximum over 16 values and
-// three shuffles: about half the instructions per row of the narrow kernel.
-// The codes follow the same steps as encode_row.
+// lane (16-byte slices), four rows per warp step: the K and V rows of two
+// consecutive tokens of one kv head.  Rows are taken head by head, tokens in
+// order, so a warp's steps advance every address by a constant (two source
+// token rows, 256 bytes of codes, two scales) and its codes land contiguously.
+// Source slices stream through shared memory with cp.async, kDepth steps
+// ahead (the bytes in flight cost no registers; each thread reads back only
+// its own slots).  The scale and every code equal encode_row's: the same
+// rounding decisions, reached with fewer instructions.
 template <bool kF32>
 __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a) {
   const int lane = threadIdx.x & 31, grp = lane >> 3, l8 = lane & 7;
-  const int64_t P = int64_t(a.N) * a.Hkv;
-  const int64_t P2 = (P + 1) >> 1;  // pair couples
+  const int64_t F = int64_t(a.N) * a.Hkv;  // rows pairs, head-major: f = h * N + t
+  const int64_t F2 = (F + 1) >> 1;          // warp steps
   const int64_t warp0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
-  const int64_t chunk = (P2 + nwarps - 1) / nwarps;
+  const int64_t chunk = (F2 + nwarps - 1) / nwarps;
   int64_t q = warp0 * chunk;
-  const int64_t qend = min(P2, q + chunk);
+  const int64_t qend = min(F2, q + chunk);
   if (q >= qend) return;
-  // this lane's pair: 2q + (grp >> 1); K for even groups, V for odd
-  int64_t p = 2 * q + (grp >> 1);
-  int t = int(p / a.Hkv), h = int(p - int64_t(t) * a.Hkv);
   const bool isv = grp & 1;
-  const void *src = isv ? a.v_src : a.k_src;
+  const char *src = static_cast<const char *>(isv ? a.v_src : a.k_src);
   int8_t *cache = isv ? a.v_cache : a.k_cache;
   __half *scale = static_cast<__half *>(isv ? a.v_scale : a.k_scale);
-  // raw source bytes of a row slice: 2 x 16 bytes (bf16) or 4 x 16 bytes (fp32)
-  constexpr int kVec = kF32 ? 4 : 2;
-  auto load = [&](int64_t pp, int tt, int hh, uint4 (&r)[kVec]) {
-    if (pp < P && SG_BOUNDS(tt < a.N && hh < a.Hkv)) {
-      const int64_t off = int64_t(tt) * a.src_tok + int64_t(hh) * a.src_head + 16 * l8;
-      const uint4 *s4 = kF32 ? reinterpret_cast<const uint4 *>(static_cast<const float *>(src) + off)
-                             : reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(src) + off);
-#pragma unroll
-      for (int u = 0; u < kVec; ++u) r[u] = s4[u];
-    } else {
-#pragma unroll
-      for (int u = 0; u < kVec; ++u) r[u] = make_uint4(0u, 0u, 0u, 0u);
+  constexpr int kVec = kF32 ? 4 : 2;  // 16-byte pieces of a 16-channel slice
+  constexpr int64_t kEsz = kF32 ? 4 : 2;
+  // A cursor over this lane's rows: f = 2 q + (grp >> 1) as (t, h), with the
+  // byte offset of its source slice.
+  struct Cursor {
+    int64_t f;
+    int t, h;
+    int64_t src;
+  };
+  auto at = [&](int64_t f) {
+    Cursor c;
+    c.f = f;
+    c.h = int(f / a.N);
+    c.t = int(f - int64_t(c.h) * a.N);
+    c.src = (int64_t(c.t) * a.src_tok + int64_t(c.h) * a.src_head + 16 * l8) * kEsz;
+    return c;
+  };
+  auto step = [&](Cursor &c) {  // f += 2
+    c.f += 2;
+    c.t += 2;
+    c.src += 2 * a.src_tok * kEsz;
+    if (c.t >= a.N) {  // next head (rare)
+      c = at(c.f);
     }
   };
-  uint4 nxt[kVec];
-  load(p, t, h, nxt);
+  constexpr int kDepth = kF32 ? 2 : 4;
+  __shared__ uint4 stage[kDepth][256][kVec];
+  Cursor ci = at(2 * q + (grp >> 1));  // issue cursor, kDepth - 1 steps ahead
+  Cursor cc = ci;                      // the step being encoded
+  auto issue = [&](int64_t qq) {
+    uint4 *slot = stage[qq % kDepth][threadIdx.x];
+    if (qq < qend && ci.f < F && SG_BOUNDS(ci.t < a.N && ci.h < a.Hkv)) {
+      const char *g4 = src + ci.src;
+#pragma unroll
+      for (int u = 0; u < kVec; ++u)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(slot + u)), "l"(g4 + 16 * u)
+                     : "memory");
+    } else {
+#pragma unroll
+      for (int u = 0; u < kVec; ++u) slot[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    if (qq < qend) step(ci);
+  };
+#pragma unroll
+  for (int i = 0; i < kDepth - 1; ++i) issue(q + i);
   for (; q < qend; ++q) {
-    // this couple's bytes; the next couple's loads are issued before the math
+    issue(q + kDepth - 1);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kDepth - 1) : "memory");
     uint4 cur[kVec];
 #pragma unroll
-    for (int u = 0; u < kVec; ++u) cur[u] = nxt[u];
-    const bool live = p < P;
-    const int tc = t, hcur = h;
-    p += 2;
-    h += 2;
-    while (h >= a.Hkv) {
-      h -= a.Hkv;
-      ++t;
-    }
-    if (q + 1 < qend) load(p, t, h, nxt);
+    for (int u = 0; u < kVec; ++u) cur[u] = stage[q % kDepth][threadIdx.x][u];
     float x[16];
     if (kF32) {
 #pragma unroll
@@ -186,7 +209,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
     }
     float amax = 0.f;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+    for (int k = 0; k < 16; k += 2) amax = fmax3(amax, fabsf(x[k]), fabsf(x[k + 1]));
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
@@ -196,43 +219,64 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
     // codes need no clamp; only fp16-subnormal scales can exceed 127.  (The
     // vote is taken by the whole warp, before any lane branches.)
     const bool clamp = __any_sync(0xffffffffu, sc > 0.f && sc < 6.103515625e-05f);
-    if (sc > 0.f) {
+    if (!clamp) {
+      // Round to nearest even by adding M = 1.5 * 2^23: the sum's ulp is 1,
+      // so fl(q + M) = M + rint(q) for |q| < 2^22, the code is the low byte of
+      // the sum's bits (two's complement), and q - (fl(q + M) - M) is exact.
+      // A q within 1e-4 of a half-integer is redone from the IEEE quotient.
+      const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;
+      const float2 M2 = make_float2(12582912.f, 12582912.f);
+      uint32_t rb[16];
+      float dmax = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; k += 2) {
+        const float2 q2 = fmul2(make_float2(x[k], x[k + 1]), make_float2(inv, inv));
+        const float2 r2 = fadd2(q2, M2);
+        const float2 d2 = fsub2(q2, fsub2(r2, M2));
+        dmax = fmax3(dmax, fabsf(d2.x), fabsf(d2.y));
+        rb[k] = __float_as_uint(r2.x);
+        rb[k + 1] = __float_as_uint(r2.y);
+      }
+      if (dmax > 0.5f - 1e-4f) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float qk = __fmul_rn(x[k], inv);
+          if (fabsf(__fsub_rn(qk, float(__float2int_rn(qk)))) > 0.5f - 1e-4f)
+            rb[k] = uint32_t(__float2int_rn(__fdiv_rn(x[k], sc)));
+        }
+      }
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4)
+        packed[k4] = __byte_perm(__byte_perm(rb[4 * k4], rb[4 * k4 + 1], 0x0040u),
+                                 __byte_perm(rb[4 * k4 + 2], rb[4 * k4 + 3], 0x0040u), 0x5410u);
+      // scale 0, NaN or infinite (flagged below): every code 0, as the IEEE path gives
+      if (!(sc > 0.f && sc <= 65504.f)) packed[0] = packed[1] = packed[2] = packed[3] = 0u;
+    } else if (sc > 0.f) {
       const float inv = __frcp_rn(sc);
-      auto encode4 = [&](int k4, auto clamp_c) {
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
         int c[4];
 #pragma unroll
-        for (int u = 0; u < 4; u += 2) {
-          const float2 q2 = fmul2(make_float2(x[4 * k4 + u], x[4 * k4 + u + 1]), make_float2(inv, inv));
-          const float qv[2] = {q2.x, q2.y};
-#pragma unroll
-          for (int v = 0; v < 2; ++v) {
-            int cv = __float2int_rn(qv[v]);  // round half to even, as rint
-            if (fabsf(__fsub_rn(qv[v], float(cv))) > 0.5f - 1e-4f)
-              cv = __float2int_rn(__fdiv_rn(x[4 * k4 + u + v], sc));
-            if (decltype(clamp_c)::value) cv = max(-127, min(127, cv));
-            c[u + v] = cv;
-          }
+        for (int u = 0; u < 4; ++u) {
+          const float qk = __fmul_rn(x[4 * k4 + u], inv);
+          int cv = __float2int_rn(qk);  // round half to even, as rint
+          if (fabsf(__fsub_rn(qk, float(cv))) > 0.5f - 1e-4f) cv = __float2int_rn(__fdiv_rn(x[4 * k4 + u], sc));
+          c[u] = max(-127, min(127, cv));
         }
         // bytes 0 of c0..c3 -> one word
-        return __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
-      };
-      if (clamp) {
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) packed[k4] = encode4(k4, std::true_type{});
-      } else {
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) packed[k4] = encode4(k4, std::false_type{});
+        packed[k4] = __byte_perm(__byte_perm(c[0], c[1], 0x0040u), __byte_perm(c[2], c[3], 0x0040u), 0x5410u);
       }
     }
-    if (live && SG_BOUNDS(tc < a.N && hcur < a.Hkv && int64_t(a.pos0) + tc < a.ncache)) {
-      const int64_t pos = int64_t(a.pos0) + tc;
-      *reinterpret_cast<uint4 *>(cache + int64_t(hcur) * a.cache_head + pos * kD + 16 * l8) =
+    if (cc.f < F && SG_BOUNDS(cc.t < a.N && cc.h < a.Hkv && int64_t(a.pos0) + cc.t < a.ncache)) {
+      const int64_t pos = int64_t(a.pos0) + cc.t;
+      *reinterpret_cast<uint4 *>(cache + int64_t(cc.h) * a.cache_head + pos * kD + 16 * l8) =
           make_uint4(packed[0], packed[1], packed[2], packed[3]);
       if (l8 == 0) {
-        scale[int64_t(hcur) * a.scale_head + pos] = s16;
+        scale[int64_t(cc.h) * a.scale_head + pos] = s16;
         if (!(fabsf(sc) <= 65504.f) && a.status) atomicCAS(a.status, 0, SAGE_ERR_NONFINITE);
       }
     }
+    step(cc);
   }
 }
 
@@ -243,12 +287,20 @@ cudaError_t launch_cache_write(const CacheWriteArgs &a, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t nrows = 2 * int64_t(a.Hkv) * a.N;
-  const int64_t want = (nrows + 7) / 8, cap = int64_t(sms) * 8;
-  const int blocks = int(want < cap ? want : cap);
   // 16-byte aligned rows (fp32 rows always are) take the wide kernel
   const int64_t esz = a.f32 ? 4 : 2;
   const bool wide = ((reinterpret_cast<uintptr_t>(a.k_src) | reinterpret_cast<uintptr_t>(a.v_src)) & 15u) == 0 &&
                     (a.src_tok * esz) % 16 == 0 && (a.src_head * esz) % 16 == 0;
+  const void *fn = wide ? (a.f32 ? reinterpret_cast<const void *>(kvc::cache_write_wide_kernel<true>)
+                                 : reinterpret_cast<const void *>(kvc::cache_write_wide_kernel<false>))
+                        : (a.f32 ? reinterpret_cast<const void *>(kvc::cache_write_kernel<true>)
+                                 : reinterpret_cast<const void *>(kvc::cache_write_kernel<false>));
+  // One wave of equal CTAs (as many as fit on the SMs at once): each warp
+  // walks one contiguous range of rows, so no partial last wave is left.
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
+  const int64_t want = (nrows + 7) / 8, cap = int64_t(sms) * per_sm;
+  const int blocks = int(want < cap ? want : cap);
   if (wide) {
     if (a.f32) kvc::cache_write_wide_kernel<true><<<blocks, 256, 0, st>>>(a);
     else kvc::cache_write_wide_kernel<false><<<blocks, 256, 0, st>>>(a);
