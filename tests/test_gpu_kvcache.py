@@ -49,7 +49,8 @@ def _check_rows(x_f32, cache, scale, pos0):
     assert (s[:, :pos0] == -1).all() and (s[:, pos0 + N:] == -1).all()
 
 
-@pytest.mark.parametrize("N,Hkv,pos0,Ncache", [(300, 3, 17, 400), (1, 1, 0, 1), (129, 8, 127, 256)])
+@pytest.mark.parametrize("N,Hkv,pos0,Ncache", [(300, 3, 17, 400), (1, 1, 0, 1), (129, 8, 127, 256),
+                                              (1, 7, 4, 6), (2, 5, 0, 2), (3, 2, 1, 4)])
 def test_cache_write_bf16_matches_oracle(cuda_lib, N, Hkv, pos0, Ncache):
     rng = np.random.default_rng(N * 31 + Hkv)
     x = (rng.standard_normal((2, N, Hkv, 128)) * rng.uniform(0.01, 40, (2, N, Hkv, 1))).astype(np.float32)
