@@ -48,6 +48,29 @@ __device__ __forceinline__ void load_row(const void *src, int64_t off, float (&x
   }
 }
 
+// fl(a / 127) without a division, by Markstein's correction step: with
+// y = fl(1/127), q0 = fl(a * y) is within an ulp of a / 127, the remainder
+// a - 127 * q0 is exact in one fma, and fl(q0 + remainder * y) is the
+// correctly rounded quotient.  Equal to IEEE division for every finite a >= 0
+// (all 2^31 such fp32 values compared on the GPU); a non-finite a gives a * y,
+// which is a / 127 (infinity or NaN) as well.
+__device__ __forceinline__ float div127(float a) {
+  const float y = 0x1.020408p-7f;  // fl(1/127)
+  const float q0 = __fmul_rn(a, y);
+  if (!(a <= 3.40282347e38f)) return q0;
+  return __fmaf_rn(__fmaf_rn(-127.f, q0, a), y, q0);
+}
+
+// The correctly rounded fp32 reciprocal of a positive finite fp16 value s:
+// the MUFU approximation refined by one Newton-Raphson step,
+// r1 = r0 + r0 (1 - s r0).  Equal to the correctly rounded 1/s for every
+// positive finite fp16 s (all 31,743 compared on the GPU).
+__device__ __forceinline__ float rcp_of_f16(float s) {
+  float r0;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(s));
+  return __fmaf_rn(r0, __fmaf_rn(-s, r0, 1.f), r0);
+}
+
 // One row of 128 channels held four per lane: fp16 scale and int8 codes.
 // q = x * fl(1/s) is within 3 * 2^-24 * |x/s| of fl(x/s); |x/s| stays below
 // 2 * 127 even for an fp16-subnormal scale, so q and fl(x/s) round to the same
@@ -58,11 +81,11 @@ __device__ __forceinline__ void encode_row(const float (&x)[4], int lane, int8_t
   float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
+  const __half s16 = __float2half_rn(div127(amax));
   const float sc = __half2float(s16);
   uint32_t packed = 0;
   if (sc > 0.f) {
-    const float inv = __frcp_rn(sc);
+    const float inv = sc <= 65504.f ? rcp_of_f16(sc) : 0.f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const float q = __fmul_rn(x[k], inv);
@@ -212,7 +235,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
     for (int k = 0; k < 16; k += 2) amax = fmax3(amax, fabsf(x[k]), fabsf(x[k + 1]));
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const __half s16 = __float2half_rn(__fdiv_rn(amax, 127.f));
+    const __half s16 = __float2half_rn(div127(amax));
     const float sc = __half2float(s16);
     uint32_t packed[4] = {0u, 0u, 0u, 0u};
     // With a normal fp16 scale (>= 2^-14), |x / s| <= 127 (1 + 2^-11), so the
@@ -224,7 +247,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
       // so fl(q + M) = M + rint(q) for |q| < 2^22, the code is the low byte of
       // the sum's bits (two's complement), and q - (fl(q + M) - M) is exact.
       // A q within 1e-4 of a half-integer is redone from the IEEE quotient.
-      const float inv = sc > 0.f ? __frcp_rn(sc) : 0.f;
+      const float inv = sc > 0.f && sc <= 65504.f ? rcp_of_f16(sc) : 0.f;
       const float2 M2 = make_float2(12582912.f, 12582912.f);
       uint32_t rb[16];
       float dmax = 0.f;
@@ -252,7 +275,7 @@ __global__ void __launch_bounds__(256) cache_write_wide_kernel(CacheWriteArgs a)
       // scale 0, NaN or infinite (flagged below): every code 0, as the IEEE path gives
       if (!(sc > 0.f && sc <= 65504.f)) packed[0] = packed[1] = packed[2] = packed[3] = 0u;
     } else if (sc > 0.f) {
-      const float inv = __frcp_rn(sc);
+      const float inv = rcp_of_f16(sc);  // fp16-subnormal scales reach this path
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
         int c[4];
