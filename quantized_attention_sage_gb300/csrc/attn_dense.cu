@@ -350,15 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         uint32_t S[128];
-        tmem_ld32(colS + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]));
-        tmem_ld32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]));
-        tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]));
-        tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]));
+        // the loads also return each 32-column slice's maximum (used when no
+        // key of the tile is masked)
+        float m32[4];
+        tmem_ld32_max(colS + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]), m32[0]);
+        tmem_ld32_max(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]), m32[1]);
+        tmem_ld32_max(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]), m32[2]);
+        tmem_ld32_max(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]), m32[3]);
         // keys of this tile that exist and, when causal, that the row may see
         const int nvalid = p.causal ? min(min(BN, p.Nk - j * BN), row + coff - j * BN + 1) : min(BN, p.Nk - j * BN);
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait(S);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) asm volatile("" : "+f"(m32[i]));
         if (p.s_dump != nullptr && SG_BOUNDS(q0 + t * BM + r < p.nq_pad && j * BN + BN <= p.nk_pad)) {
           // diagnostic copy of the exact integer scores
           int32_t *d = p.s_dump + (int64_t(bh) * p.nq_pad + (q0 + t * BM + r)) * p.nk_pad + j * BN;
@@ -386,18 +391,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 128; ++i)
               if (i >= nvalid) Sf[i] = -INFINITY;
           }
-          // row maximum of the raw scores, four independent chains
-          float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
-          float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
+          // row maximum of the raw scores: from the loads for a full tile,
+          // four independent chains over the masked scores otherwise
+          float mlo, mhi;
+          if (!kMasked) {
+            mlo = fmaxf(m32[0], m32[1]);
+            mhi = fmaxf(m32[2], m32[3]);
+          } else {
+            float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
+            float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
 #pragma unroll
-          for (int i = 3; i < 31; i += 2) {
-            c0 = fmax3(c0, Sf[i], Sf[i + 1]);
-            c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
-            c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
-            c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
+            for (int i = 3; i < 31; i += 2) {
+              c0 = fmax3(c0, Sf[i], Sf[i + 1]);
+              c1 = fmax3(c1, Sf[32 + i], Sf[33 + i]);
+              c2 = fmax3(c2, Sf[64 + i], Sf[65 + i]);
+              c3 = fmax3(c3, Sf[96 + i], Sf[97 + i]);
+            }
+            mlo = fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]);
+            mhi = fmax3(fmax3(c2, c3, Sf[95]), Sf[127], Sf[127]);
           }
-          const float mlo = fmax3(fmax3(c0, c1, Sf[31]), Sf[63], Sf[63]);
-          const float mhi = fmax3(fmax3(c2, c3, Sf[95]), Sf[127], Sf[127]);
           float mt;
           if (kMasked) {
             mt = fmaxf(mlo == -INFINITY ? -INFINITY : __fmul_rn(mlo, t_lo),
