@@ -19,22 +19,27 @@
 // chunk c+2, so that neither the copies nor the short quantizer launches
 // sit between two attention launches.  Inputs, outputs and the quantized
 // intermediates (codes, scales, images) are double-buffered in the caller's
-// workspace (slot c % 2).  Cross-stream order comes from events created for
-// the call (timing disabled) and released as soon as they are enqueued.
+// workspace (slot c % 2), and so are the events that order the streams.
 //
 // Per chunk c (slot s = c % 2), in stream order:
 //   staging: H2D q, k, v -> in[s]; prepare in[s] -> images[s], codes[s];
-//            record q_ready[c]
-//   compute: wait q_ready[c]; attention kernel on images[s], codes[s] -> out[s];
-//            record done[c]
-//   staging: wait done[c]; D2H out[s]; prepare chunk c+2 into images[s], codes[s]
+//            record q_ready[s]
+//   compute: wait q_ready[s]; attention kernel on images[s], codes[s] -> out[s];
+//            record done[s]
+//   staging: wait done[s]; D2H out[s]; prepare chunk c+2 into images[s], codes[s]
 // H2D of chunk c+2 is queued before the wait for done[c]: in[s] was last read
 // by the preparation of chunk c, earlier on the same stream.  The preparation
 // of chunk c+2 follows done[c] (images[s] have been read) and D2H of chunk c
-// (out[s] is drained before attention(c+2), which waits for q_ready[c+2]).
+// (out[s] is drained before attention(c+2), which waits for q_ready[s] as
+// recorded for chunk c+2).
 // The staging stream first waits for the work already queued on the compute
 // stream; at the end the compute stream waits for the last D2H, so the caller
-// synchronises one stream.
+// synchronises one stream.  The cross-stream order uses six events (q_ready
+// and done as two-slot rings, start, last), created once per thread and device
+// context and reused by every call: recording an event again is safe because
+// every wait on its previous record has been enqueued by then.  (Creating and
+// destroying events in every call made the device stall for ~40 ms about once
+// per thousand events created.)
 #include <cuda_runtime.h>
 
 #include <vector>
@@ -44,6 +49,36 @@
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// The six events of sage_attention_host for the calling thread and the current
+// device context (created on first use; a context created again after a reset
+// gets new ones).
+struct HostEvents {
+  unsigned long long ctx = 0;
+  cudaEvent_t ev[6] = {};
+};
+cudaError_t host_events(cudaEvent_t (&out)[6]) {
+  thread_local HostEvents cache[sg::CtxOnce::kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= sg::CtxOnce::kDevices) return cudaErrorInvalidDevice;
+  HostEvents &h = cache[dev];
+  const unsigned long long ctx = sg::current_context_id();
+  if (ctx == 0) return cudaErrorDeviceUninitialized;  // no current context
+  if (h.ctx != ctx) {  // first use here, or the context was destroyed with its events
+    for (cudaEvent_t &x : h.ev) {
+      e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+      if (e != cudaSuccess) {
+        h.ctx = 0;
+        return e;
+      }
+    }
+    h.ctx = ctx;
+  }
+  for (int i = 0; i < 6; ++i) out[i] = h.ev[i];
+  return cudaSuccess;
+}
 
 size_t up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -214,8 +249,6 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
 
   const std::vector<int> first = chunk_starts(B * H, L.hc);
   const int C = int(first.size()) - 1;
-  std::vector<cudaEvent_t> q_ready(C, nullptr), done(C, nullptr);
-  cudaEvent_t start = nullptr, last = nullptr;
   sage_status st = SAGE_OK;
   auto fail = [&](sage_status s) {
     if (st == SAGE_OK) st = s;
@@ -224,12 +257,10 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     if (e != cudaSuccess) fail(SAGE_ERR_CUDA);
     return e == cudaSuccess;
   };
-  for (int c = 0; c < C && st == SAGE_OK; ++c) {
-    ck(cudaEventCreateWithFlags(&q_ready[c], cudaEventDisableTiming));
-    ck(cudaEventCreateWithFlags(&done[c], cudaEventDisableTiming));
-  }
-  if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&last, cudaEventDisableTiming));
-  if (st == SAGE_OK) ck(cudaEventCreateWithFlags(&start, cudaEventDisableTiming));
+  cudaEvent_t evs[6];
+  if (!ck(host_events(evs))) return st;
+  cudaEvent_t *q_ready = evs, *done = evs + 2;  // slot c & 1 for head group c
+  cudaEvent_t start = evs[4], last = evs[5];
   // the staging stream starts after everything already queued on the compute
   // stream (e.g. a previous call that used the same workspace)
   if (st == SAGE_OK && ck(cudaEventRecord(start, cs))) ck(cudaStreamWaitEvent(xs, start, 0));
@@ -263,7 +294,7 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
       fail(r);
       return;
     }
-    if (st == SAGE_OK) ck(cudaEventRecord(q_ready[c], xs));
+    if (st == SAGE_OK) ck(cudaEventRecord(q_ready[c & 1], xs));
   };
   for (int c = 0; c < 2 && c < C && st == SAGE_OK; ++c) {
     h2d(c);
@@ -271,7 +302,7 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
   }
   for (int c = 0; c < C && st == SAGE_OK; ++c) {
     const int s = c & 1, n = heads_of(c);
-    if (!ck(cudaStreamWaitEvent(cs, q_ready[c], 0))) break;
+    if (!ck(cudaStreamWaitEvent(cs, q_ready[c & 1], 0))) break;
     // the attention kernel alone (arguments checked above; images written by the staging stream)
     sg::DenseArgs a;
     a.q_codes = nullptr;  // the attention reads the images
@@ -295,21 +326,14 @@ sage_status sage_attention_host(const void *q_host, const void *k_host, const vo
     a.causal = causal;
     a.images_ready = true;
     if (!ck(sg::launch_attn_dense(a, cs))) break;
-    if (!ck(cudaEventRecord(done[c], cs))) break;
+    if (!ck(cudaEventRecord(done[c & 1], cs))) break;
     if (c + 2 < C) h2d(c + 2);  // in[s] was last read by quantize(c), earlier on this stream
-    if (st != SAGE_OK || !ck(cudaStreamWaitEvent(xs, done[c], 0))) break;
+    if (st != SAGE_OK || !ck(cudaStreamWaitEvent(xs, done[c & 1], 0))) break;
     ck(cudaMemcpyAsync(static_cast<uint8_t *>(out_host) + size_t(first[c]) * qrow, ws + L.off_out[s], n * qrow,
                        cudaMemcpyDeviceToHost, xs));
     if (c + 2 < C && st == SAGE_OK) quantize(c + 2);
   }
   if (st == SAGE_OK && ck(cudaEventRecord(last, xs))) ck(cudaStreamWaitEvent(cs, last, 0));
-  // events still pending on the device are released once they complete
-  for (int c = 0; c < C; ++c) {
-    if (q_ready[c]) cudaEventDestroy(q_ready[c]);
-    if (done[c]) cudaEventDestroy(done[c]);
-  }
-  if (last) cudaEventDestroy(last);
-  if (start) cudaEventDestroy(start);
   return st;
 }
 
