@@ -37,9 +37,8 @@
 // synchronises one stream.  The cross-stream order uses six events (q_ready
 // and done as two-slot rings, start, last), created once per thread and device
 // context and reused by every call: recording an event again is safe because
-// every wait on its previous record has been enqueued by then.  (Creating and
-// destroying events in every call made the device stall for ~40 ms about once
-// per thousand events created.)
+// every wait on its previous record has been enqueued by then, and a call
+// then creates and destroys no driver objects.
 #include <cuda_runtime.h>
 
 #include <vector>
