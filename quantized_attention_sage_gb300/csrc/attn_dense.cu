@@ -350,20 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         uint32_t S[128];
-        // the loads also return each 32-column slice's maximum (used when no
-        // key of the tile is masked)
-        float m32[4];
-        tmem_ld32_max(colS + 0, *reinterpret_cast<uint32_t(*)[32]>(&S[0]), m32[0]);
-        tmem_ld32_max(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&S[32]), m32[1]);
-        tmem_ld32_max(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(&S[64]), m32[2]);
-        tmem_ld32_max(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(&S[96]), m32[3]);
+        // the two loads also return the maximum of each 64-key half (used
+        // when no key of the tile is masked)
+        float mh[2];
+        tmem_ld64_max(colS + 0, *reinterpret_cast<uint32_t(*)[64]>(&S[0]), mh[0]);
+        tmem_ld64_max(colS + 64, *reinterpret_cast<uint32_t(*)[64]>(&S[64]), mh[1]);
         // keys of this tile that exist and, when causal, that the row may see
         const int nvalid = p.causal ? min(min(BN, p.Nk - j * BN), row + coff - j * BN + 1) : min(BN, p.Nk - j * BN);
         float nt_lo = 0.f, nt_hi = 0.f;  // next tile's multipliers, loaded while S is in flight
         if (j + 1 < T) tile_t(j + 1, nt_lo, nt_hi);
         tmem_ld_wait(S);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) asm volatile("" : "+f"(m32[i]));
+        asm volatile("" : "+f"(mh[0]), "+f"(mh[1]));
         if (p.s_dump != nullptr && SG_BOUNDS(q0 + t * BM + r < p.nq_pad && j * BN + BN <= p.nk_pad)) {
           // diagnostic copy of the exact integer scores
           int32_t *d = p.s_dump + (int64_t(bh) * p.nq_pad + (q0 + t * BM + r)) * p.nk_pad + j * BN;
@@ -395,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // four independent chains over the masked scores otherwise
           float mlo, mhi;
           if (!kMasked) {
-            mlo = fmaxf(m32[0], m32[1]);
-            mhi = fmaxf(m32[2], m32[3]);
+            mlo = mh[0];
+            mhi = mh[1];
           } else {
             float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[32], Sf[33], Sf[34]);
             float c2 = fmax3(Sf[64], Sf[65], Sf[66]), c3 = fmax3(Sf[96], Sf[97], Sf[98]);
