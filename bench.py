@@ -56,13 +56,13 @@ WORKLOAD = "videodit_b1h24n37810"
 
 # DRAM bytes (read + write) per launch of the attention kernel, from one ncu
 # capture of the 24-head, 16,384-token case (the fp16 images exceed L2 there):
-# 251.8 MB read + 72.2 MB written, scaled by 37,810 / 16,384 (every head's
+# 251.9 MB read + 72.3 MB written, scaled by 37,810 / 16,384 (every head's
 # inputs are read once, so the bytes grow with heads x tokens); and the kernel's
 # tensor-pipe activity from the full ncu capture of the 8,192-token case.  Both
 # hold for the kernel source with this sha256 prefix and are None once the
 # source has changed.
-TRAFFIC = {"sha256_prefix": "358b6502801a57d8", "bytes": (251.8e6 + 72.2e6) * 37810 / 16384,
-           "tensor_pipe_active": 0.505}
+TRAFFIC = {"sha256_prefix": "c6fc3dfc76c26d4b", "bytes": (251.9e6 + 72.3e6) * 37810 / 16384,
+           "tensor_pipe_active": 0.511}
 # algorithmic bytes of one attention launch at the full workload: Q, K, V codes
 # (1 byte per element) and the bf16 output
 ATTN_METHOD_BYTES = 24 * 37810 * 128 * (1 + 1 + 1 + 2)
