@@ -569,7 +569,10 @@ def run_ours(args, rank, world):
     # ---- end to end through the public API with pinned host buffers: sage_attention_host
     # copies groups of heads in and out on a copy stream while the previous group runs
     hout = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(2, min(args.steps, 8))
+    # about half a second of timed steps, so that the mean takes in proportion,
+    # not all or nothing, the 40-80 ms stalls that sustained host-buffer calls
+    # can show about every 0.5 s
+    e2e_steps = max(2, min(5 * args.steps, 50))
     head_chunk = 6
     cstream, xstream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ws_host = torch.empty(L.sage_attention_host_workspace(B, H, N, N, head_chunk), dtype=torch.uint8, device=dev)
@@ -604,6 +607,7 @@ def run_ours(args, rank, world):
     ms_e2e = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     per_step = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(e2e_steps)]
     e2e = {"value": whole_job_tflops(w.flops, world, ms_e2e), "unit": UNIT, "ms_per_step": ms_e2e,
+           "ms_median_step": statistics.median(per_step), "steps": e2e_steps,
            "ms_each_step": per_step, "host_enqueue_ms_each_step": enqueue_ms,
            "h2d_bytes_per_step": 3 * q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2,
            "api": f"sage_attention_host, head_chunk={head_chunk}, pinned host buffers"}
