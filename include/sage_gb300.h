@@ -25,8 +25,10 @@
  *    tensors whose channel stride is 1; every stride and base pointer must be
  *    16-byte aligned (strides are multiples of 8 elements for bf16).
  *  - Inputs must be finite.  The functions hold no global state (except the
- *    scratch array of sage_quantize_qk_noalloc) and may be called from several
- *    host threads.
+ *    scratch array of sage_quantize_qk_noalloc, and the six CUDA events that
+ *    sage_attention_host creates per calling thread and device context on its
+ *    first call and reuses afterwards) and may be called from several host
+ *    threads.
  *
  * Citations name the page and its section that defines each operation.
  */
@@ -289,7 +291,9 @@ sage_status sage_attention(const void *q_bf16, sage_strides qs, const void *k_bf
  *     also runs the quantizer kernels).  Everything is
  *     enqueued asynchronously; out_host is complete once compute_stream has
  *     reached the end of the call (it waits for the last copy).  The copies
- *     start after the work already queued on compute_stream.
+ *     start after the work already queued on compute_stream.  The two streams
+ *     are ordered by six events that the calling thread keeps for its current
+ *     device context (created by the first call, reused by every later one).
  * Errors as the three entry points; SAGE_ERR_INVALID_ARG for a null pointer,
  * head_chunk < 1 or equal streams.  After an error, work already enqueued may
  * still run: synchronise both streams before reusing the buffers.
