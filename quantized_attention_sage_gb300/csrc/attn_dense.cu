@@ -16,10 +16,9 @@
 //    swizzled shared memory; S (double-buffered) and O live in TMEM.
 //  * One CTA owns two 128-row query tiles of one (b, h); every K/V tile read
 //    serves both.  (When the last wave of CTAs would leave more than half of
-//    the SMs idle, its pairs run as single-tile CTAs instead.)  Warp 0 issues TMA; warps 1 and 3 issue Q.K^T of tile 0
-//    and tile 1, warp 2 issues both P.V (tcgen05.mma issue blocks for about
-//    one MMA's execution and slows the softmax warps of the issuing
-//    sub-partition, so the issue is spread); warps 4-7 and 8-11 are two
+//    the SMs idle, its pairs run as single-tile CTAs instead.)  Warp 0 issues
+//    TMA; warps 1 and 3 issue Q.K^T of tile 0 and tile 1, warp 2 issues both
+//    P.V (one issuing warp per sub-partition); warps 4-7 and 8-11 are two
 //    softmax warpgroups, one per query tile, one query row per thread (TMEM
 //    lane = row).  TMEM: S0, S1, O0, O1, 128 columns each.  The role
 //    warpgroup hands registers to the softmax warpgroups (setmaxnreg).
@@ -30,10 +29,13 @@
 //  * The two softmax warps of a sub-partition take turns for the arithmetic
 //    (one computes while the other loads S, stores P or rescales O).
 //  * Softmax per element: row max on the raw int32-valued S (the dequant
-//    multiplier is positive, so max(fl(S*t)) = fl(max(S)*t)), one FFMA for
-//    S*t - m' + log2(448), ex2 on MUFU (448*p directly), fp32 row sums of
-//    448*p, E4M3 conversion of 448*p; the ex2 of one group of keys are
-//    issued between the sums and conversions of the previous group.
+//    multiplier is positive, so max(fl(S*t)) = fl(max(S)*t)); for a key tile
+//    with no masked key it comes with the two 64-column S loads
+//    (tcgen05.ld.red with .max returns the values and each half's maximum,
+//    one per 64-key scale block).  Then one FFMA for S*t - m' + log2(448), ex2
+//    on MUFU (448*p directly), fp32 row sums of 448*p, E4M3 conversion of
+//    448*p; the ex2 of one group of keys are issued between the sums and
+//    conversions of the previous group.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
