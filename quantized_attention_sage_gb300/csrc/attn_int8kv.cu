@@ -23,10 +23,13 @@
 //    with tcgen05.st over the consumed S buffer and read by the MMA from TMEM.
 //  * Four softmax warpgroups, one per 32-key quarter of every key tile, one
 //    query row per thread: four warps per SM sub-partition.  They share one
-//    O accumulator and one running max per row: each quarter's maximum is
-//    exchanged through shared memory under a named barrier of the four warps
-//    that hold the same rows, so every warpgroup uses the exact row maximum,
-//    and each rescales its own 32 columns of O.
+//    O accumulator and one reference maximum per row: each quarter's maximum
+//    is exchanged through shared memory under a named barrier of the four
+//    warps that hold the same rows, and each rescales its own 32 columns of O.
+//    The reference is the exact maximum of the first tile; later tiles take
+//    their weights against the kept reference before the exchange and are
+//    redone only when their maximum passes it by more than 15 (the weights
+//    are fp16 hi + lo, whose range holds 2^15).
 //  * S is double-buffered in TMEM and QK(j+2) is issued right behind PV(j),
 //    so the next scores are ready when the softmax finishes a tile; the MMA
 //    and TMA warps run converged with one elected lane issuing.
@@ -318,18 +321,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = p.q_pos0 + qi;  // keys 0..pos are visible
     const uint32_t lane_base = tmem + (uint32_t(quad * 32) << 16);
     const uint32_t colO = lane_base + kColO + kQuarter * g;  // this quarter's 32 columns of O
-    // w = p * vs * 2^-E with 2^E > max vs: w < 1 stays well inside fp16.  The
-    // factor 2^-E is taken into the exponent (p' = 2^(s - m - E)), so the row
-    // sum is l * 2^-E as well and O / l is unchanged.
+    // w = p * vs * 2^-E with 2^E > max vs: w < p = 2^(s - m), which stays
+    // inside fp16 while s - m <= 15.  The factor 2^-E is taken into the
+    // exponent (p' = 2^(s - m - E)), so the row sum is l * 2^-E as well and
+    // O / l is unchanged.
     const float vmax = __uint_as_float(*p.vmax_bits);
     const int E = vmax > 0.f ? int((__float_as_uint(vmax) >> 23) & 0xFF) - 127 + 1 : 0;
     const float Ef = float(E);
-    float m = -INFINITY, l = 0.f;  // m: the row's running max (same in all quarters); l: this quarter's sum
+    float m = -INFINITY, l = 0.f;  // m: the row's reference maximum (same in all quarters); l: this quarter's sum
     bool ok = true;
     // Named barriers cannot time out, so every warp of a quadrant passes
     // exactly T + 1 of them (one per tile and one at the end), also after a
     // bounded wait gave up: a warp that left the loop early makes up the
     // ones it skipped, without work, so that the others are never stranded.
+    // All of them are the reducing form (bar.red), which must not be mixed
+    // with bar.sync on the same barrier.
     int nbar = 0;
     if (g == 0) {
       // Q into TMEM: row r's 128 bf16 (two 128-byte swizzled rows of the TMA
@@ -398,10 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < kQuarter; ++i)
             if (i >= nvis) Sf[i] = -INFINITY;
         }
-        // the quarter's maximum (two chains), then the row's over all four
-        // quarters: the four warps holding these rows meet at named barrier
-        // 1 + quad; xm is double-buffered by tile, and no warp can be two
-        // tiles ahead of another since each tile has such a barrier
+        // the quarter's maximum (two chains)
         float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[16], Sf[17], Sf[18]);
 #pragma unroll
         for (int i = 3; i < 15; i += 2) {
@@ -409,62 +412,98 @@ __global__ void __launch_bounds__(kThreads, 1)
           c1 = fmax3(c1, Sf[16 + i], Sf[17 + i]);
         }
         const float mq = fmax3(fmax3(c0, c1, Sf[15]), Sf[31], Sf[31]);
-        reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
-        named_bar_sync(1 + quad, 128);
-        ++nbar;
-        const float4 mx = xm[b * BM + r];
-        const float mt = fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w));
-        mnew = fmaxf(m, mt);
-        alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : ex2(__fsub_rn(m, mnew));
-        // x = s - (m' + E); masked entries stay -inf (p' = 0)
-        const float nb = (mnew == -INFINITY) ? 0.f : __fadd_rn(mnew, Ef);
-        const float2 nb2 = make_float2(nb, nb);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-        // p' = 2^x, row sum, w = p' * vs split into fp16 hi + lo, written over
-        // this quarter's S columns: hi at +0..15, lo at +16..31
+        // the row's maximum over the four quarters of the tile: the four warps
+        // holding these rows meet at named barrier 1 + quad; xm is
+        // double-buffered by tile, and no warp can be two tiles ahead of
+        // another since each tile has exactly one such barrier
+        auto tile_max = [&]() -> float {
+          reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
+          named_bar_or(1 + quad, 128, false);
+          ++nbar;
+          const float4 mx = xm[b * BM + r];
+          return fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w));
+        };
+        // p' = 2^(s - nb) with nb = reference + E, the row sum, and w = p' * vs
+        // split into fp16 hi + lo, written over this quarter's S columns: hi
+        // at +0..15, lo at +16..31; returns the quarter's row sum
+        auto weights = [&](float nb) -> float {
+          const float2 nb2 = make_float2(nb, nb);
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t hi[8], lo[8];
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hi[8], lo[8];
 #pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const int e = 16 * c + i;
-            const float4 v4 = vs4[e >> 2];
-            const float2 x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
-            const float2 x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
-            const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-            const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-            acc0 = fadd2(acc0, p01);
-            acc1 = fadd2(acc1, p23);
-            const float2 w01 = fmul2(p01, make_float2(v4.x, v4.y));
-            const float2 w23 = fmul2(p23, make_float2(v4.z, v4.w));
-            // hi = w with its mantissa cut to fp16's 10 bits (exact in fp16
-            // for w >= 2^-14; below that fp16 rounds it, an absolute error
-            // under 2^-25), lo = w - hi exactly in fp32, then rounded to fp16
-            const float2 t01 = make_float2(__uint_as_float(__float_as_uint(w01.x) & 0xFFFFE000u),
-                                           __uint_as_float(__float_as_uint(w01.y) & 0xFFFFE000u));
-            const float2 t23 = make_float2(__uint_as_float(__float_as_uint(w23.x) & 0xFFFFE000u),
-                                           __uint_as_float(__float_as_uint(w23.y) & 0xFFFFE000u));
-            const __half2 h01 = __floats2half2_rn(t01.x, t01.y);
-            const __half2 h23 = __floats2half2_rn(t23.x, t23.y);
-            const float2 r01 = fsub2(w01, t01);
-            const float2 r23 = fsub2(w23, t23);
-            const __half2 l01 = __floats2half2_rn(r01.x, r01.y);
-            const __half2 l23 = __floats2half2_rn(r23.x, r23.y);
-            hi[i >> 1] = *reinterpret_cast<const uint32_t *>(&h01);
-            hi[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-            lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
-            lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+            for (int i = 0; i < 16; i += 4) {
+              const int e = 16 * c + i;
+              const float4 v4 = vs4[e >> 2];
+              const float2 x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
+              const float2 x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
+              const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+              const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+              acc0 = fadd2(acc0, p01);
+              acc1 = fadd2(acc1, p23);
+              const float2 w01 = fmul2(p01, make_float2(v4.x, v4.y));
+              const float2 w23 = fmul2(p23, make_float2(v4.z, v4.w));
+              // hi = w with its mantissa cut to fp16's 10 bits (exact in fp16
+              // for w >= 2^-14; below that fp16 rounds it, an absolute error
+              // under 2^-25), lo = w - hi exactly in fp32, then rounded to fp16
+              const float2 t01 = make_float2(__uint_as_float(__float_as_uint(w01.x) & 0xFFFFE000u),
+                                             __uint_as_float(__float_as_uint(w01.y) & 0xFFFFE000u));
+              const float2 t23 = make_float2(__uint_as_float(__float_as_uint(w23.x) & 0xFFFFE000u),
+                                             __uint_as_float(__float_as_uint(w23.y) & 0xFFFFE000u));
+              const __half2 h01 = __floats2half2_rn(t01.x, t01.y);
+              const __half2 h23 = __floats2half2_rn(t23.x, t23.y);
+              const float2 r01 = fsub2(w01, t01);
+              const float2 r23 = fsub2(w23, t23);
+              const __half2 l01 = __floats2half2_rn(r01.x, r01.y);
+              const __half2 l23 = __floats2half2_rn(r23.x, r23.y);
+              hi[i >> 1] = *reinterpret_cast<const uint32_t *>(&h01);
+              hi[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h23);
+              lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
+              lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+            }
+            tmem_st8(sa + 8 * c, hi);
+            tmem_st8(sa + 16 + 8 * c, lo);
           }
-          tmem_st8(sa + 8 * c, hi);
-          tmem_st8(sa + 16 + 8 * c, lo);
+          return __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+        };
+        // The reference maximum m of the weights.  While some row of the warp
+        // has none, the tile's maximum is exchanged first and becomes it.
+        // After that the reference is kept: the tile's weights are taken
+        // against it at once and the exchange follows them, so the
+        // exponentials do not wait for it.  The weights are fp16 hi + lo, not
+        // FP8, so a reference below the tile's maximum only scales them (O / l
+        // does not change), and up to 2^15 they stay inside fp16 (w < 2^(s - m),
+        // since vs * 2^-E < 1).  A tile whose maximum passes the reference by
+        // more than 15 is redone against the new running maximum, and O and l
+        // are rescaled.  All four warps of a quadrant hold the same rows, the
+        // same m and the same exchanged maxima, so they take the same branch.
+        if (__any_sync(0xffffffffu, m == -INFINITY)) {
+          mnew = fmaxf(m, tile_max());
+          // x = s - (m' + E); masked entries stay -inf (p' = 0)
+          rowsum = weights(mnew == -INFINITY ? 0.f : __fadd_rn(mnew, Ef));
+        } else {
+          rowsum = weights(__fadd_rn(m, Ef));
+          mnew = m;
+          // the exchange: the barrier itself reports whether any quarter of
+          // any row of the quadrant passed the reference by more than 15; the
+          // maxima are read back only then
+          reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
+          ++nbar;
+          if (named_bar_or(1 + quad, 128, mq > __fadd_rn(m, 15.f))) {
+            const float4 mx = xm[b * BM + r];
+            mnew = fmaxf(m, fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w)));
+            tmem_st_wait();  // the first weights are written before they are replaced
+            rowsum = weights(__fadd_rn(mnew, Ef));
+          }
         }
-        rowsum = __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
+        alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : (mnew == m ? 1.f : ex2(__fsub_rn(m, mnew)));
       };
       if (__any_sync(0xffffffffu, nvis < kQuarter)) softmax_quarter(std::true_type{});
       else softmax_quarter(std::false_type{});
       l = __fadd_rn(__fmul_rn(alpha, l), rowsum);
       // O is stable once the P.V of tile j-1 is complete; this quarter's
-      // warps rescale their 32 columns of it when the row max grew
+      // warps rescale their 32 columns of it when the reference moved
       if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
         ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort, p.wait_ns);
         if (!ok) break;
@@ -491,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // L = l_0 + l_1 + l_2 + l_3 in quarter order; every quarter writes its 32
     // channels of the partial O, quarter 0 also (m, L)
     if (ok) reinterpret_cast<float *>(&xl[r])[g] = l;
-    for (; nbar <= T; ++nbar) named_bar_sync(1 + quad, 128);
+    for (; nbar <= T; ++nbar) named_bar_or(1 + quad, 128, false);
     if (!ok) {
       report(p.status, SAGE_ERR_TIMEOUT);
     } else {

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_output_close, bf16_to_f64
+from gpu_helpers import assert_output_close, assert_output_close_rows, bf16_to_f64
 from kv_helpers import both_caches
 
 pytestmark = pytest.mark.gpu
@@ -105,6 +105,38 @@ def test_int8kv_full_size_whole_kv_group(cuda_lib, name):
     max_abs, rel = assert_output_close(got, ref_b, f"{name} kv group {g}")
     print(f"{name} kv group {g}: {rows.size} rows, max-abs {max_abs:.2e} rel-L2 {rel:.2e}; "
           f"vs unrounded fp64 rel-L2 {np.linalg.norm(got - ref) / np.linalg.norm(ref):.2e}")
+
+
+def test_int8kv_late_dominant_keys(cuda_lib):
+    """Keys far above everything before them, in key tiles after the first of a
+    split piece: in every kv head the keys at four positions are 20 x one query
+    vector of that head group, so that query's row (and about half of the
+    others) sees a logit tens to hundreds of units of log2 above the maximum
+    of the earlier tiles.  Every row against the fp64 oracle, at the bar for
+    rows that one or two keys dominate (their outputs are of order one, where a
+    bf16 step is 2^-7 to 2^-5: rel-L2 <= 1e-3 and every element within
+    max(2e-3, one bf16 step of the oracle's value)); the aligned rows of the
+    oracle return that key's dequantised V."""
+    w = synth.Int8KVWorkload("kv_late_spikes", 9, 256, 2048, 32, 8, sub=14)
+    x = synth.int8kv_inputs(w)
+    G = w.Hq // w.Hkv
+    qv = oracle.bf16_value(x["q"])  # [Nq, Hq, 128]
+    aligned = []
+    for g in range(w.Hkv):
+        for i, pos in enumerate((300, 777, 1500, 1900)):
+            row, head = 40 * i + 7, g * G + i % G
+            assert pos <= w.q_pos0 + row  # visible to the aligned query
+            x["k_raw"][g, pos] = (20.0 * qv[row, head]).astype(np.float32)
+            aligned.append((row, head, g, pos))
+    host, out = run(cuda_lib, w, x)
+    rows, heads = np.meshgrid(np.arange(w.Nq), np.arange(w.Hq), indexing="ij")
+    ref_b, ref = oracle_bf16(w, host, rows.ravel(), heads.ravel())
+    got = bf16_to_f64(out).reshape(-1, 128)
+    assert_output_close_rows(got, ref_b, w.name)
+    for row, head, g, pos in aligned:
+        v_deq = host["v"][g, pos].astype(np.float64) * float(host["v_scale"][g, pos])
+        k = row * w.Hq + head
+        assert np.abs(ref[k] - v_deq).max() < 1e-6 * max(1.0, np.abs(v_deq).max())
 
 
 def test_int8kv_quarter_million_token_cache_sampled(cuda_lib):
