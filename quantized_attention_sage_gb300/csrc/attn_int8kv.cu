@@ -15,8 +15,9 @@
 //    memory take all of its bandwidth while they run, and the TMA copies of
 //    the next K/V tiles and the scale loads share it.
 //  * softmax per row in fp32: s = S * fl(ks * sm_scale * log2 e), causal mask
-//    by absolute position, p = 2^(s - m).
-//  * P.V: the weight w = p * vs (scaled by a power of two so that w < 1) is
+//    by absolute position, p = 2^(s - m) with the exponent taken from the raw
+//    score in one FMA (S * kt - (m + E)) once the row has a reference m.
+//  * P.V: the weight w = p * vs (scaled by a power of two so that w < 2^15) is
 //    split into fp16 hi + lo parts and multiplied with exact fp16 images of the
 //    V codes by one K = 256 kind::f16 MMA chain ([hi | lo] . [V ; V]), so the
 //    fp16 rounding of w does not reach the output.  hi and lo are written
@@ -388,56 +389,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the diagonal carry no per-element predicates.
       auto softmax_quarter = [&](auto masked_c) {
         constexpr bool kMasked = decltype(masked_c)::value;
-        // s = S * kt (base-2 logits)
-#pragma unroll
-        for (int i = 0; i < kQuarter; i += 4) {
-          const float4 k4 = kt4[i >> 2];
-          const float2 a = fmul2(make_float2(Sf[i], Sf[i + 1]), make_float2(k4.x, k4.y));
-          const float2 c = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
-          Sf[i] = a.x;
-          Sf[i + 1] = a.y;
-          Sf[i + 2] = c.x;
-          Sf[i + 3] = c.y;
-        }
-        if (kMasked) {  // keys past the query's position
-#pragma unroll
-          for (int i = 0; i < kQuarter; ++i)
-            if (i >= nvis) Sf[i] = -INFINITY;
-        }
-        // the quarter's maximum (two chains)
-        float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[16], Sf[17], Sf[18]);
-#pragma unroll
-        for (int i = 3; i < 15; i += 2) {
-          c0 = fmax3(c0, Sf[i], Sf[i + 1]);
-          c1 = fmax3(c1, Sf[16 + i], Sf[17 + i]);
-        }
-        const float mq = fmax3(fmax3(c0, c1, Sf[15]), Sf[31], Sf[31]);
-        // the row's maximum over the four quarters of the tile: the four warps
-        // holding these rows meet at named barrier 1 + quad; xm is
-        // double-buffered by tile, and no warp can be two tiles ahead of
-        // another since each tile has exactly one such barrier
-        auto tile_max = [&]() -> float {
-          reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
-          named_bar_or(1 + quad, 128, false);
-          ++nbar;
-          const float4 mx = xm[b * BM + r];
-          return fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w));
-        };
-        // p' = 2^(s - nb) with nb = reference + E, the row sum, and w = p' * vs
-        // split into fp16 hi + lo, written over this quarter's S columns: hi
-        // at +0..15, lo at +16..31; returns the quarter's row sum
-        auto weights = [&](float nb) -> float {
-          const float2 nb2 = make_float2(nb, nb);
+        // p' = 2^x, the row sum, and w = p' * vs split into fp16 hi + lo,
+        // written over this quarter's S columns: hi at +0..15, lo at +16..31;
+        // returns the quarter's row sum.  x = s - nb (nb = reference + E):
+        // from the base-2 logits already in Sf (kRaw false), or from the raw
+        // scores in one FMA, x = S * kt - nb (kRaw true), which also gives
+        // the quarter's largest x in xq (masked keys are -inf)
+        auto weights = [&](float nb, auto raw_c, float &xq) -> float {
+          constexpr bool kRaw = decltype(raw_c)::value;
+          const float2 nb2 = make_float2(nb, nb), nbn2 = make_float2(-nb, -nb);
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          float q0 = -INFINITY, q1 = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t hi[8], lo[8];
 #pragma unroll
             for (int i = 0; i < 16; i += 4) {
               const int e = 16 * c + i;
-              const float4 v4 = vs4[e >> 2];
-              const float2 x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
-              const float2 x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
+              const float4 v4 = lds_f4_in_order(vs4 + (e >> 2));
+              float2 x01, x23;
+              if (kRaw) {
+                const float4 k4 = lds_f4_in_order(kt4 + (e >> 2));
+                x01 = ffma2(make_float2(Sf[e], Sf[e + 1]), make_float2(k4.x, k4.y), nbn2);
+                x23 = ffma2(make_float2(Sf[e + 2], Sf[e + 3]), make_float2(k4.z, k4.w), nbn2);
+                if (kMasked) {  // keys past the query's position
+                  if (e >= nvis) x01.x = -INFINITY;
+                  if (e + 1 >= nvis) x01.y = -INFINITY;
+                  if (e + 2 >= nvis) x23.x = -INFINITY;
+                  if (e + 3 >= nvis) x23.y = -INFINITY;
+                }
+                q0 = fmax3(q0, x01.x, x01.y);
+                q1 = fmax3(q1, x23.x, x23.y);
+              } else {
+                x01 = fsub2(make_float2(Sf[e], Sf[e + 1]), nb2);
+                x23 = fsub2(make_float2(Sf[e + 2], Sf[e + 3]), nb2);
+              }
               const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
               const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
               acc0 = fadd2(acc0, p01);
@@ -465,36 +451,69 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st8(sa + 8 * c, hi);
             tmem_st8(sa + 16 + 8 * c, lo);
           }
+          xq = fmaxf(q0, q1);
           return __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
         };
         // The reference maximum m of the weights.  While some row of the warp
-        // has none, the tile's maximum is exchanged first and becomes it.
-        // After that the reference is kept: the tile's weights are taken
-        // against it at once and the exchange follows them, so the
-        // exponentials do not wait for it.  The weights are fp16 hi + lo, not
-        // FP8, so a reference below the tile's maximum only scales them (O / l
-        // does not change), and up to 2^15 they stay inside fp16 (w < 2^(s - m),
-        // since vs * 2^-E < 1).  A tile whose maximum passes the reference by
-        // more than 15 is redone against the new running maximum, and O and l
-        // are rescaled.  All four warps of a quadrant hold the same rows, the
-        // same m and the same exchanged maxima, so they take the same branch.
+        // has none, the tile's exact maximum is exchanged first (the four
+        // warps holding these rows meet at named barrier 1 + quad; xm is
+        // double-buffered by tile, and no warp can be two tiles ahead of
+        // another since each tile has exactly one such barrier) and becomes
+        // it.  After that the reference is kept: the tile's weights are taken
+        // against it at once, from the raw scores, and the exchange follows
+        // them, so the exponentials do not wait for it.  The weights are fp16
+        // hi + lo, not FP8, so a reference below the tile's maximum only
+        // scales them (O / l does not change), and up to 2^15 they stay inside
+        // fp16 (w < 2^(s - m), since vs * 2^-E < 1).  A tile whose maximum
+        // passes the reference by more than 15 (x > 15 - E) is redone against
+        // the new running maximum, and O and l are rescaled.  All four warps
+        // of a quadrant hold the same rows, the same m and the same exchanged
+        // maxima, so they take the same branch.
+        float xq;
         if (__any_sync(0xffffffffu, m == -INFINITY)) {
-          mnew = fmaxf(m, tile_max());
+          // s = S * kt (base-2 logits), masked, and the quarter's maximum
+#pragma unroll
+          for (int i = 0; i < kQuarter; i += 4) {
+            const float4 k4 = kt4[i >> 2];
+            const float2 a = fmul2(make_float2(Sf[i], Sf[i + 1]), make_float2(k4.x, k4.y));
+            const float2 c = fmul2(make_float2(Sf[i + 2], Sf[i + 3]), make_float2(k4.z, k4.w));
+            Sf[i] = a.x;
+            Sf[i + 1] = a.y;
+            Sf[i + 2] = c.x;
+            Sf[i + 3] = c.y;
+          }
+          if (kMasked) {
+#pragma unroll
+            for (int i = 0; i < kQuarter; ++i)
+              if (i >= nvis) Sf[i] = -INFINITY;
+          }
+          float c0 = fmax3(Sf[0], Sf[1], Sf[2]), c1 = fmax3(Sf[16], Sf[17], Sf[18]);
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) {
+            c0 = fmax3(c0, Sf[i], Sf[i + 1]);
+            c1 = fmax3(c1, Sf[16 + i], Sf[17 + i]);
+          }
+          reinterpret_cast<float *>(&xm[b * BM + r])[g] = fmax3(fmax3(c0, c1, Sf[15]), Sf[31], Sf[31]);
+          named_bar_or(1 + quad, 128, false);
+          ++nbar;
+          const float4 mx = xm[b * BM + r];
+          mnew = fmaxf(m, fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w)));
           // x = s - (m' + E); masked entries stay -inf (p' = 0)
-          rowsum = weights(mnew == -INFINITY ? 0.f : __fadd_rn(mnew, Ef));
+          rowsum = weights(mnew == -INFINITY ? 0.f : __fadd_rn(mnew, Ef), std::false_type{}, xq);
         } else {
-          rowsum = weights(__fadd_rn(m, Ef));
+          const float nb = __fadd_rn(m, Ef);
+          rowsum = weights(nb, std::true_type{}, xq);
           mnew = m;
           // the exchange: the barrier itself reports whether any quarter of
           // any row of the quadrant passed the reference by more than 15; the
-          // maxima are read back only then
-          reinterpret_cast<float *>(&xm[b * BM + r])[g] = mq;
+          // quarter maxima (as logits, xq + nb) are read back only then
+          reinterpret_cast<float *>(&xm[b * BM + r])[g] = __fadd_rn(xq, nb);
           ++nbar;
-          if (named_bar_or(1 + quad, 128, mq > __fadd_rn(m, 15.f))) {
+          if (named_bar_or(1 + quad, 128, xq > 15.f - Ef)) {
             const float4 mx = xm[b * BM + r];
             mnew = fmaxf(m, fmaxf(fmaxf(mx.x, mx.y), fmaxf(mx.z, mx.w)));
             tmem_st_wait();  // the first weights are written before they are replaced
-            rowsum = weights(__fadd_rn(mnew, Ef));
+            rowsum = weights(__fadd_rn(mnew, Ef), std::true_type{}, xq);
           }
         }
         alpha = (m == -INFINITY) ? (mnew == -INFINITY ? 1.f : 0.f) : (mnew == m ? 1.f : ex2(__fsub_rn(m, mnew)));

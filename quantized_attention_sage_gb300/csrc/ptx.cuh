@@ -244,6 +244,16 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// A 16-byte shared-memory load that stays in program order among the other
+// volatile asm statements (plain loads of an unrolled loop are all hoisted to
+// its top, which costs registers where they are scarce).
+__device__ __forceinline__ float4 lds_f4_in_order(const void *p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(p)));
+  return v;
+}
 // The same barrier, returning the OR of `pred` over the participating threads.
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
   uint32_t r;
