@@ -390,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto softmax_quarter = [&](auto masked_c) {
         constexpr bool kMasked = decltype(masked_c)::value;
         // p' = 2^x, the row sum, and w = p' * vs split into fp16 hi + lo,
-        // written over this quarter's S columns: hi at +0..15, lo at +16..31;
+        // written over this quarter's S columns: hi at +0..15, lo at +16..31,
+        // in blocks of 8 keys (4 columns each: fewer registers live at once);
         // returns the quarter's row sum.  x = s - nb (nb = reference + E):
         // from the base-2 logits already in Sf (kRaw false), or from the raw
         // scores in one FMA, x = S * kt - nb (kRaw true), which also gives
@@ -401,11 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           float q0 = -INFINITY, q1 = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t hi[8], lo[8];
+          for (int c = 0; c < 4; ++c) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const int e = 16 * c + i;
+            for (int i = 0; i < 8; i += 4) {
+              const int e = 8 * c + i;
               const float4 v4 = lds_f4_in_order(vs4 + (e >> 2));
               float2 x01, x23;
               if (kRaw) {
@@ -448,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
               lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
             }
-            tmem_st8(sa + 8 * c, hi);
-            tmem_st8(sa + 16 + 8 * c, lo);
+            tmem_st4(sa + 4 * c, hi);
+            tmem_st4(sa + 16 + 4 * c, lo);
           }
           xq = fmaxf(q0, q1);
           return __fadd_rn(__fadd_rn(acc0.x, acc0.y), __fadd_rn(acc1.x, acc1.y));
