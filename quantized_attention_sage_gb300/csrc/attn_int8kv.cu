@@ -111,6 +111,23 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
+// Two weights w (fp32, below 2^15) as fp16 pairs hi + lo: hi = fp16_rn(w),
+// lo = fp16_rn(w - hi).  w - hi is exact in fp32 (hi keeps the leading 11
+// bits of w, or w's fp16-subnormal grid), taken in one mixed-precision FMA
+// per weight (fp32 = fp16 * fp16 + fp32: hi * -1 + w), so hi + lo is w to
+// within 2^-22 relative (2^-25 absolute below fp16's normal range).  Pairs
+// in the bf16x2/f16x2 order: the first weight in the low half.
+__device__ __forceinline__ void split_f16(float2 w, uint32_t &hi, uint32_t &lo) {
+  asm("{\n\t.reg .b16 a, b, m;\n\t.reg .f32 ra, rb;\n\t"
+      "mov.b16 m, 0xBC00;\n\t"
+      "cvt.rn.f16x2.f32 %0, %3, %2;\n\t"
+      "mov.b32 {a, b}, %0;\n\t"
+      "fma.rn.f32.f16 ra, a, m, %2;\n\t"
+      "fma.rn.f32.f16 rb, b, m, %3;\n\t"
+      "cvt.rn.f16x2.f32 %1, rb, ra;\n\t}"
+      : "=r"(hi), "=r"(lo)
+      : "f"(w.x), "f"(w.y));
+}
 __device__ __forceinline__ void report(int32_t *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
@@ -431,23 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc1 = fadd2(acc1, p23);
               const float2 w01 = fmul2(p01, make_float2(v4.x, v4.y));
               const float2 w23 = fmul2(p23, make_float2(v4.z, v4.w));
-              // hi = w with its mantissa cut to fp16's 10 bits (exact in fp16
-              // for w >= 2^-14; below that fp16 rounds it, an absolute error
-              // under 2^-25), lo = w - hi exactly in fp32, then rounded to fp16
-              const float2 t01 = make_float2(__uint_as_float(__float_as_uint(w01.x) & 0xFFFFE000u),
-                                             __uint_as_float(__float_as_uint(w01.y) & 0xFFFFE000u));
-              const float2 t23 = make_float2(__uint_as_float(__float_as_uint(w23.x) & 0xFFFFE000u),
-                                             __uint_as_float(__float_as_uint(w23.y) & 0xFFFFE000u));
-              const __half2 h01 = __floats2half2_rn(t01.x, t01.y);
-              const __half2 h23 = __floats2half2_rn(t23.x, t23.y);
-              const float2 r01 = fsub2(w01, t01);
-              const float2 r23 = fsub2(w23, t23);
-              const __half2 l01 = __floats2half2_rn(r01.x, r01.y);
-              const __half2 l23 = __floats2half2_rn(r23.x, r23.y);
-              hi[i >> 1] = *reinterpret_cast<const uint32_t *>(&h01);
-              hi[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&h23);
-              lo[i >> 1] = *reinterpret_cast<const uint32_t *>(&l01);
-              lo[(i >> 1) + 1] = *reinterpret_cast<const uint32_t *>(&l23);
+              split_f16(w01, hi[i >> 1], lo[i >> 1]);
+              split_f16(w23, hi[(i >> 1) + 1], lo[(i >> 1) + 1]);
             }
             tmem_st4(sa + 4 * c, hi);
             tmem_st4(sa + 16 + 4 * c, lo);
